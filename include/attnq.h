@@ -1,0 +1,199 @@
+/*
+ * attnq - causal FP8 (E4M3) attention forward with the numerics options of
+ * the attention-numerics pages, for GB300 (sm_103a).
+ *
+ * Sources (page titles and sections):
+ *  [AN] "attention-numerics" project page, method and kernel settings:
+ *       per-(batch, head) Q/K/V scales over the full sequence; the same
+ *       Hadamard transform on Q and K, never V; mean-key subtraction keeps
+ *       exact attention; ideal causal FP64 attention as the reference.
+ *  [RR] "A rounding problem, not a rotation problem", 01 / Synthetic
+ *       illustration (one maximum-based FP8 scale, fixed random-sign
+ *       Hadamard, E4M3FN round-to-nearest-even saturating at +-448, mean
+ *       subtraction before rotation) and 02 / Measured heads
+ *       (log(1 + relative Frobenius error) per head).
+ *  [PC] "Technische Samenvatting: P-Cast Precisie in FP8 Attention", sec. 1
+ *       (online softmax over KV blocks forward 0->N or reverse N->0; static
+ *       scale S multiplied into P before the E4M3 cast and divided out in the
+ *       epilogue) and sec. 3-4 (kernel-faithful simulation: Q, K, V in FP32,
+ *       only P cast).
+ *
+ * Conventions for every call:
+ *  - Tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *    16-byte aligned, in the layouts stated below.  The library keeps no
+ *    allocation between calls and allocates none during a call; scratch
+ *    memory comes from the caller's workspace.
+ *  - Calls are asynchronous on `stream`.  The return value reports argument
+ *    and launch errors found before or at launch.  Errors found on the device
+ *    (non-finite input, a wait that timed out) are recorded in a per-device
+ *    status word and reported by attnq_device_status().
+ *  - No C++ exception crosses this interface.  Functions are thread-safe for
+ *    distinct streams except where stated.
+ *  - Requires an sm_103 device; other devices give ATTNQ_EUNSUPPORTED.
+ */
+#ifndef ATTNQ_H_
+#define ATTNQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTNQ_OK = 0,
+  ATTNQ_EINVAL = 1,        /* bad argument: null pointer, bad size, misaligned, workspace too small */
+  ATTNQ_EUNSUPPORTED = 2,  /* valid but not supported here: d, kv_tile, device */
+  ATTNQ_ECUDA = 3,         /* a CUDA runtime/driver call failed */
+  ATTNQ_ENONFINITE = 4,    /* a NaN or infinity in an input (or produced by the transform) */
+  ATTNQ_ETIMEOUT = 5       /* a device-side wait gave up (the kernel returned early) */
+} attnq_status;
+
+/* desc.flags */
+enum { ATTNQ_ROTATE = 1u, ATTNQ_CENTER_K = 2u, ATTNQ_VT_LAYOUT = 4u };
+/* element types of Q/K/V inputs and of O */
+enum { ATTNQ_F32 = 0, ATTNQ_BF16 = 1 };
+/* KV-tile visiting order of the online softmax [PC sec. 1] */
+enum { ATTNQ_KV_FORWARD = 0, ATTNQ_KV_REVERSE = 1 };
+
+/*
+ * Problem description.  Q is [B, Hq, N, d]; K and V are [B, Hkv, N, d];
+ * query head h reads KV head h / (Hq / Hkv) (Hq must be a multiple of Hkv).
+ * d is 64 or 128.  in_dtype is ATTNQ_F32 or ATTNQ_BF16 (inputs of
+ * attnq_prepare).  flags:
+ *   ATTNQ_ROTATE    multiply Q and K rows by `signs` and apply the
+ *                   unnormalised fast Walsh-Hadamard transform [AN], [RR];
+ *   ATTNQ_CENTER_K  subtract from K the mean key of its (batch, KV head) over
+ *                   all N tokens, before rotation [AN], [RR];
+ *   ATTNQ_VT_LAYOUT v8 is stored transposed, [B, Hkv, d, ldv] with
+ *                   ldv = attnq_vt_ld(N) (tokens N .. ldv-1 are zero).
+ * signs: DEVICE pointer to d int8 values, each +1 or -1; required when
+ * ATTNQ_ROTATE is set, ignored otherwise.
+ */
+typedef struct {
+  int32_t B, Hq, Hkv, N, d;
+  int32_t in_dtype;
+  uint32_t flags;
+  const int8_t* signs;
+} attnq_desc;
+
+/*
+ * Per-(batch, head) descales (amax / 448, fp32) written by attnq_prepare and
+ * read by attnq_fwd: q_descale [B*Hq], k_descale and v_descale [B*Hkv].
+ * k_mean: optional [B*Hkv*d] fp32 output of the mean key (may be NULL).
+ */
+typedef struct {
+  float* q_descale;
+  float* k_descale;
+  float* v_descale;
+  float* k_mean;
+} attnq_scales;
+
+/* Library version: major*10000 + minor*100 + patch. */
+int32_t attnq_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char* attnq_status_string(attnq_status s);
+
+/*
+ * Row length in bytes of the transposed V layout: N rounded up to 16
+ * (TMA needs 16-byte row strides).  Returns 0 for N <= 0.
+ */
+int64_t attnq_vt_ld(int32_t N);
+
+/*
+ * Fixed random signs for the Hadamard rotation [RR: "fixed random-sign
+ * Hadamard"]: sign c is -1 when bit 63 of SplitMix64 output c+1 of stream
+ * `seed` is set, else +1.  Writes d values to HOST memory host_out.
+ */
+attnq_status attnq_hadamard_signs(uint64_t seed, int32_t d, int8_t* host_out);
+
+/* Bytes of device workspace attnq_prepare needs for `desc` (0 on a bad desc). */
+size_t attnq_prepare_workspace(const attnq_desc* desc);
+
+/*
+ * Operand preparation [AN], [RR]: for every (batch, head) slice of Q, K, V
+ *   1. upcast to fp32;
+ *   2. K only, with ATTNQ_CENTER_K: subtract the mean key mu (fp32; per
+ *      channel, 128-token chunks summed in token order, chunk sums added in
+ *      chunk order, one IEEE division by N);
+ *   3. Q and K only, with ATTNQ_ROTATE: x <- FWHT(signs * x), unnormalised,
+ *      butterfly stages h = 1, 2, ..., d/2;
+ *   4. amax = max |x| over the slice; descale = amax/448 and qs = 448/amax
+ *      (IEEE fp32 division; 1 and 1 when amax == 0);
+ *   5. x8 = E4M3 code of fl32(x * qs), round-to-nearest-even, saturating.
+ * Q, K, V: DEVICE, in_dtype elements, [B,H,N,d].  q8 [B,Hq,N,d], k8
+ * [B,Hkv,N,d]: DEVICE uint8 E4M3 codes.  v8: [B,Hkv,N,d], or
+ * [B,Hkv,d,attnq_vt_ld(N)] with ATTNQ_VT_LAYOUT.  out: descales (and the
+ * optional mean key) as DEVICE pointers.  workspace: DEVICE, at least
+ * attnq_prepare_workspace(desc) bytes, 256-byte aligned; its contents need no
+ * initialisation and are garbage afterwards.  A non-finite value in an input
+ * slice (or produced by its transform) sets ATTNQ_ENONFINITE in the device
+ * status; outputs are then unspecified.
+ */
+attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K, const void* V, uint8_t* q8,
+                           uint8_t* k8, uint8_t* v8, const attnq_scales* out, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/*
+ * Causal FP8 attention forward [AN], [PC sec. 1]: for each query row i and
+ * the KV tiles of width kv_tile (aligned at token 0) holding a key j <= i
+ * (every key when causal == 0), visited forward (0 -> diagonal) or reverse
+ * (diagonal -> 0):
+ *   s_j = q8_i . k8_j (exact products, fp32 accumulation);
+ *   t_j = s_j * c,  c = fl32(dq * dk / sqrt(d) * (ROTATE ? 1/d : 1) * log2 e);
+ *   m' = max(m, max_j t_j);  alpha = 2^(m - m');  P_j = 2^(t_j - m');
+ *   l = alpha * l + sum_j P_j;  p8_j = E4M3(P_j * S);
+ *   acc = alpha * acc + sum_j p8_j * v8_j;
+ * and finally O = acc * dv / (S * l).  The running maximum is exact (no
+ * lazy rescaling).  desc: shape and flags of the attnq_prepare call that made
+ * the operands (ATTNQ_VT_LAYOUT is required; in_dtype is ignored).
+ * q8, k8, v8, scales: DEVICE, as written by attnq_prepare.  S: finite, in
+ * (0, 448].  kv_order: ATTNQ_KV_FORWARD or ATTNQ_KV_REVERSE.  kv_tile: 64 or
+ * 128.  O: DEVICE [B,Hq,N,d] of out_dtype (ATTNQ_F32 or ATTNQ_BF16, RNE).
+ * underflow_opt: NULL, or DEVICE uint64 [B*Hq*2] that the call ADDS to:
+ * [2*bh] counts in-mask keys j >= k_sink of KV tile 0 whose P*S > 0 was cast
+ * to 0, [2*bh+1] the same over all later tiles [PC sec. 1-2].
+ */
+attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                       const attnq_scales* scales, float S, int32_t kv_order, int32_t causal, int32_t kv_tile,
+                       void* O, int32_t out_dtype, uint64_t* underflow_opt, int32_t k_sink, cudaStream_t stream);
+
+/*
+ * P-only ("kernel-faithful simulation") forward [PC sec. 3-4]: the loop of
+ * attnq_fwd on fp32 Q [B,Hq,N,d], K, V [B,Hkv,N,d] (DEVICE) with fp32 dot
+ * products, c = fl32(log2 e / sqrt(d)), only P cast to E4M3, O = acc/(S*l)
+ * (DEVICE fp32 [B,Hq,N,d]).  desc.flags and desc.in_dtype are ignored.
+ * Other arguments as attnq_fwd.  d is 64 or 128; kv_tile 16..128, a
+ * multiple of 16.
+ */
+attnq_status attnq_fwd_ponly(const attnq_desc* desc, const float* Q, const float* K, const float* V, float S,
+                             int32_t kv_order, int32_t causal, int32_t kv_tile, float* O, uint64_t* underflow_opt,
+                             int32_t k_sink, cudaStream_t stream);
+
+/*
+ * Per-head error [RR, 02 / Measured heads]: err[bh] = log1p(||O - O_ref||_F
+ * / ||O_ref||_F) over the N*d outputs of head bh, with both squared norms
+ * accumulated in fp64.  O: DEVICE [B,Hq,N,d] of o_dtype; O_ref: DEVICE fp64
+ * [B,Hq,N,d]; err_out: DEVICE fp64 [B*Hq] (overwritten).  A head with
+ * ||O_ref|| = 0 gives 0 when O equals O_ref there, else +infinity.
+ */
+attnq_status attnq_err(const attnq_desc* desc, const void* O, int32_t o_dtype, const double* O_ref,
+                       double* err_out, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: ATTNQ_OK, ATTNQ_ENONFINITE or ATTNQ_ETIMEOUT (the
+ * first error recorded since the last call), or ATTNQ_ECUDA when the
+ * synchronisation itself failed.  Not thread-safe against kernels of this
+ * library running on other streams of the same device.
+ */
+attnq_status attnq_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNQ_H_ */

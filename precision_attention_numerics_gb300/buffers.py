@@ -1,0 +1,33 @@
+"""Device buffers for one prepare/forward call (torch allocations only)."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+from .binding import ATTNQ_VT_LAYOUT, AttnqDesc, AttnqScales, attnq_prepare_workspace, attnq_vt_ld
+
+
+@dataclass
+class PreparedBuffers:
+    q8: object
+    k8: object
+    v8: object
+    scales: AttnqScales
+    workspace: object
+
+
+def alloc_prepared(desc: AttnqDesc, device="cuda", with_mean: bool = True) -> PreparedBuffers:
+    """E4M3 operand tensors, descales, optional mean key and workspace for `desc`."""
+    import torch
+    B, Hq, Hkv, N, d = desc.B, desc.Hq, desc.Hkv, desc.N, desc.d
+    q8 = torch.empty((B, Hq, N, d), dtype=torch.uint8, device=device)
+    k8 = torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=device)
+    if desc.flags & ATTNQ_VT_LAYOUT:
+        v8 = torch.empty((B, Hkv, d, attnq_vt_ld(N)), dtype=torch.uint8, device=device)
+    else:
+        v8 = torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=device)
+    scales = AttnqScales(torch.empty(B * Hq, dtype=torch.float32, device=device),
+                         torch.empty(B * Hkv, dtype=torch.float32, device=device),
+                         torch.empty(B * Hkv, dtype=torch.float32, device=device),
+                         torch.empty(B * Hkv * d, dtype=torch.float32, device=device) if with_mean else None)
+    ws = torch.empty(max(attnq_prepare_workspace(desc), 256), dtype=torch.uint8, device=device)
+    return PreparedBuffers(q8, k8, v8, scales, ws)

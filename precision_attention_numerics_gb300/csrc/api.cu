@@ -1,0 +1,273 @@
+// C ABI of libattnq: argument validation, workspace carve-up, tensor maps,
+// launches and the device status word.  Declarations and their contracts are
+// in include/attnq.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attnq.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attnq {
+
+__device__ uint32_t g_status;  // DEV_* bits, one word per device
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+bool g_sm103[kMaxDevices] = {};
+std::mutex g_mu;
+
+// Per-device set-up: the status word's device address, SM count and
+// architecture check.  Done once per device with that device current.
+attnq_status device_setup(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTNQ_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ATTNQ_EUNSUPPORTED;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_status_ptr[dev]) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTNQ_ECUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return ATTNQ_ECUDA;
+    g_sm103[dev] = (major == 10 && minor == 3);
+    g_num_sms[dev] = sms;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_sm103[dev] ? ATTNQ_OK : ATTNQ_EUNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attnq_status check_desc(const attnq_desc* d) {
+  if (!d) return ATTNQ_EINVAL;
+  if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0 || d->d <= 0) return ATTNQ_EINVAL;
+  if (d->Hq % d->Hkv != 0) return ATTNQ_EINVAL;
+  if ((d->flags & ~uint32_t(ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT)) != 0) return ATTNQ_EINVAL;
+  if (d->d != 64 && d->d != 128) return ATTNQ_EUNSUPPORTED;
+  // grid.y of the prepare passes and int32 indices of rows
+  const int64_t nslices = int64_t(d->B) * d->Hq + 2 * int64_t(d->B) * d->Hkv;
+  if (nslices > 65535) return ATTNQ_EUNSUPPORTED;
+  if (int64_t(d->N) * d->d > (int64_t(1) << 31)) return ATTNQ_EUNSUPPORTED;
+  return ATTNQ_OK;
+}
+
+attnq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTNQ_OK : ATTNQ_ECUDA; }
+
+uint64_t g_wait_ns = 2000000000ull;  // 2 s per mbarrier wait
+
+}  // namespace
+
+namespace {
+// cuTensorMapEncodeTiled is looked up through the runtime, so the library
+// does not link the driver library directly (and loads on hosts without one).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+CUresult encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                         CUtensorMapSwizzle swizzle) {
+  const EncodeTiledFn fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace attnq
+
+using namespace attnq;
+
+extern "C" {
+
+int32_t attnq_version(void) { return 100; }
+
+const char* attnq_status_string(attnq_status s) {
+  switch (s) {
+    case ATTNQ_OK: return "ATTNQ_OK";
+    case ATTNQ_EINVAL: return "ATTNQ_EINVAL: invalid argument";
+    case ATTNQ_EUNSUPPORTED: return "ATTNQ_EUNSUPPORTED: unsupported size, option or device";
+    case ATTNQ_ECUDA: return "ATTNQ_ECUDA: CUDA call failed";
+    case ATTNQ_ENONFINITE: return "ATTNQ_ENONFINITE: non-finite input";
+    case ATTNQ_ETIMEOUT: return "ATTNQ_ETIMEOUT: device wait timed out";
+  }
+  return "unknown attnq status";
+}
+
+int64_t attnq_vt_ld(int32_t N) { return N <= 0 ? 0 : (int64_t(N) + 15) / 16 * 16; }
+
+attnq_status attnq_hadamard_signs(uint64_t seed, int32_t d, int8_t* host_out) {
+  if (!host_out || d <= 0) return ATTNQ_EINVAL;
+  for (int32_t c = 0; c < d; ++c) {
+    uint64_t z = seed + uint64_t(c + 1) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z = z ^ (z >> 31);
+    host_out[c] = (z >> 63) ? int8_t(-1) : int8_t(1);
+  }
+  return ATTNQ_OK;
+}
+
+size_t attnq_prepare_workspace(const attnq_desc* desc) {
+  if (check_desc(desc) != ATTNQ_OK) return 0;
+  return prepare_workspace_bytes(desc->B, desc->Hq, desc->Hkv, desc->N, desc->d,
+                                 (desc->flags & ATTNQ_CENTER_K) ? 1 : 0);
+}
+
+attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K, const void* V, uint8_t* q8,
+                           uint8_t* k8, uint8_t* v8, const attnq_scales* out, void* workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (desc->in_dtype != ATTNQ_F32 && desc->in_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  if (!Q || !K || !V || !q8 || !k8 || !v8 || !out || !out->q_descale || !out->k_descale || !out->v_descale)
+    return ATTNQ_EINVAL;
+  if ((desc->flags & ATTNQ_ROTATE) && !desc->signs) return ATTNQ_EINVAL;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(q8) || !aligned16(k8) || !aligned16(v8))
+    return ATTNQ_EINVAL;
+  const size_t need = attnq_prepare_workspace(desc);
+  if (!workspace || ws_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTNQ_EINVAL;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  PrepareArgs a{};
+  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d;
+  a.bf16 = desc->in_dtype == ATTNQ_BF16;
+  a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
+  a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
+  a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
+  a.signs = desc->signs;
+  a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
+  a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
+  a.ldv = attnq_vt_ld(desc->N);
+  a.status = g_status_ptr[dev];
+  carve_prepare_workspace(a, workspace);
+  return from_cuda(launch_prepare(a, stream));
+}
+
+attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                       const attnq_scales* scales, float S, int32_t kv_order, int32_t causal, int32_t kv_tile,
+                       void* O, int32_t out_dtype, uint64_t* underflow_opt, int32_t k_sink, cudaStream_t stream) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (!q8 || !k8 || !v8 || !scales || !scales->q_descale || !scales->k_descale || !scales->v_descale || !O)
+    return ATTNQ_EINVAL;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(O)) return ATTNQ_EINVAL;
+  if (!(std::isfinite(S) && S > 0.0f && S <= 448.0f)) return ATTNQ_EINVAL;
+  if (kv_order != ATTNQ_KV_FORWARD && kv_order != ATTNQ_KV_REVERSE) return ATTNQ_EINVAL;
+  if (causal != 0 && causal != 1) return ATTNQ_EINVAL;
+  if (out_dtype != ATTNQ_F32 && out_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  if (k_sink < 0) return ATTNQ_EINVAL;
+  if (kv_tile != 64 && kv_tile != 128) return ATTNQ_EUNSUPPORTED;
+  if (!(desc->flags & ATTNQ_VT_LAYOUT)) return ATTNQ_EUNSUPPORTED;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  FwdArgs a{};
+  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d; a.T = kv_tile;
+  a.causal = causal; a.reverse = kv_order == ATTNQ_KV_REVERSE;
+  a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
+  a.S = S;
+  a.q8 = q8; a.k8 = k8; a.v8t = v8; a.ldv = attnq_vt_ld(desc->N);
+  a.q_ds = scales->q_descale; a.k_ds = scales->k_descale; a.v_ds = scales->v_descale;
+  a.O = O; a.out_bf16 = out_dtype == ATTNQ_BF16;
+  a.underflow = reinterpret_cast<unsigned long long*>(underflow_opt);
+  a.k_sink = k_sink;
+  a.status = g_status_ptr[dev];
+  a.wait_ns = g_wait_ns;
+  a.num_sms = g_num_sms[dev];
+  return from_cuda(launch_fwd(a, stream));
+}
+
+attnq_status attnq_fwd_ponly(const attnq_desc* desc, const float* Q, const float* K, const float* V, float S,
+                             int32_t kv_order, int32_t causal, int32_t kv_tile, float* O, uint64_t* underflow_opt,
+                             int32_t k_sink, cudaStream_t stream) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (!Q || !K || !V || !O) return ATTNQ_EINVAL;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return ATTNQ_EINVAL;
+  if (!(std::isfinite(S) && S > 0.0f && S <= 448.0f)) return ATTNQ_EINVAL;
+  if (kv_order != ATTNQ_KV_FORWARD && kv_order != ATTNQ_KV_REVERSE) return ATTNQ_EINVAL;
+  if (causal != 0 && causal != 1) return ATTNQ_EINVAL;
+  if (k_sink < 0) return ATTNQ_EINVAL;
+  if (kv_tile < 16 || kv_tile > 128 || kv_tile % 16) return ATTNQ_EUNSUPPORTED;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  PonlyArgs a{};
+  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d; a.T = kv_tile;
+  a.causal = causal; a.reverse = kv_order == ATTNQ_KV_REVERSE;
+  a.S = S;
+  a.Q = Q; a.K = K; a.V = V; a.O = O;
+  a.underflow = reinterpret_cast<unsigned long long*>(underflow_opt);
+  a.k_sink = k_sink;
+  return from_cuda(launch_ponly(a, stream));
+}
+
+attnq_status attnq_err(const attnq_desc* desc, const void* O, int32_t o_dtype, const double* O_ref,
+                       double* err_out, cudaStream_t stream) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (!O || !O_ref || !err_out) return ATTNQ_EINVAL;
+  if (o_dtype != ATTNQ_F32 && o_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  ErrArgs a{};
+  a.n_heads = desc->B * desc->Hq;
+  a.per_head = int64_t(desc->N) * desc->d;
+  a.O = O;
+  a.o_bf16 = o_dtype == ATTNQ_BF16;
+  a.O_ref = O_ref;
+  a.err = err_out;
+  return from_cuda(launch_err(a, stream));
+}
+
+attnq_status attnq_device_status(cudaStream_t stream) {
+  int dev;
+  attnq_status st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTNQ_ECUDA;
+  uint32_t bits = 0;
+  if (cudaMemcpy(&bits, g_status_ptr[dev], sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTNQ_ECUDA;
+  if (bits) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(g_status_ptr[dev], &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return ATTNQ_ECUDA;
+  }
+  if (bits & DEV_NONFINITE) return ATTNQ_ENONFINITE;
+  if (bits & DEV_TIMEOUT) return ATTNQ_ETIMEOUT;
+  return ATTNQ_OK;
+}
+
+}  // extern "C"

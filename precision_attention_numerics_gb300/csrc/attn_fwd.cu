@@ -1,0 +1,591 @@
+// Causal FP8 (E4M3) attention forward on tcgen05 tensor cores.
+//
+// Method ("attention-numerics" project page, method and kernel settings;
+// "Technische Samenvatting: P-Cast Precisie in FP8 Attention", sec. 1):
+// per query row, KV tiles of width T are visited forward (0 -> diagonal) or
+// reverse (diagonal -> 0); per tile
+//   t_j = (q8 . k8_j) * c,  m' = max(m, max_j t_j),  alpha = 2^(m - m'),
+//   P_j = 2^(t_j - m'),  l = alpha*l + sum_j P_j,  p8_j = E4M3(P_j * S),
+//   O_acc = alpha*O_acc + sum_j p8_j v8_j;   O = O_acc * dv / (S * l).
+// The running maximum is exact; O is rescaled whenever alpha != 1 (a
+// skipped rescale with alpha == 1 is exact).
+//
+// Work unit: one 128-row query tile of two query heads that share a KV head
+// (GQA); both use the same K/V tiles and the same KV range.  A persistent
+// grid walks the units longest-first (query tiles nearest the end of the
+// sequence have the most KV tiles).
+//
+// CTA = 320 threads:
+//   warps 0-3  softmax warpgroup 0 (query head h0), TMEM lanes 0..127 = rows
+//   warps 4-7  softmax warpgroup 1 (query head h0 + 1)
+//   warp 8     TMA producer: Q tiles once per unit, K and V^T tiles through
+//              an NS-stage ring
+//   warp 9     TMEM allocator and MMA issuer (one thread)
+// TMEM columns: S_w at [w*T, w*T+T) (P_w overwrites its first T/4 columns as
+// packed E4M3, the A operand of the P.V MMA), O_w at [2T + w*D, 2T + w*D + D).
+// Per tile and warpgroup w the MMA thread issues S_w = Q_w K^T
+// (kind::f8f6f4, M=128, N=T, K=32 per instruction), the softmax warpgroup
+// turns S_w into P_w, then the MMA thread issues O_w += P_w V (A from TMEM,
+// M=128, N=D) followed at once by S_w for the next tile, so warpgroup 1's
+// softmax overlaps warpgroup 0's MMAs and the other way round.
+//
+// Every mbarrier wait is bounded; on a timeout the CTA records
+// DEV_TIMEOUT, every role leaves its loop, outstanding TMA loads and MMAs are
+// drained (again with a bound) and TMEM is freed before the CTA exits.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attnq {
+namespace {
+
+constexpr int kRows = 128;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+
+struct Params {
+  int B, Hq, Hkv, N, G, pairs, n_qt, n_units;
+  int causal, reverse;
+  float S;
+  const float* q_ds;
+  const float* k_ds;
+  const float* v_ds;
+  double inv_sqrt_d, rot, log2e;
+  void* O;
+  int out_bf16;
+  unsigned long long* uf;
+  int k_sink;
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+template <int D, int T>
+struct Cfg {
+  static constexpr int QB = kRows * D;  // bytes of one Q tile
+  static constexpr int KB = T * D;      // bytes of one K stage
+  static constexpr int VB = D * T;      // bytes of one V^T stage
+  static constexpr int NS0 = (196608 - 2 * QB) / (KB + VB);
+  static constexpr int NS = NS0 > 6 ? 6 : NS0;
+  static constexpr int COLS_USED = 2 * T + 2 * D;
+  static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256u : 512u;
+  static constexpr uint32_t LAYOUT_QK = D == 128 ? 2u : 4u;  // 128B / 64B swizzle
+  static constexpr uint32_t SBO_QK = 8u * D;
+  static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;
+  static constexpr uint32_t SBO_V = 8u * T;
+  static constexpr int NBARS = 2 + 4 * NS + 8 + 1;
+  static constexpr size_t SMEM = 1024 + 2 * size_t(QB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
+  static_assert(COLS_USED <= 512, "TMEM budget");
+};
+
+struct Unit {
+  int t, b, g, h0, nact, nt;
+};
+
+template <int T>
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+  const int per_t = p.B * p.Hkv * p.pairs;
+  Unit un;
+  un.t = p.n_qt - 1 - u / per_t;
+  int r = u % per_t;
+  un.b = r / (p.Hkv * p.pairs);
+  r %= p.Hkv * p.pairs;
+  un.g = r / p.pairs;
+  const int pr = r % p.pairs;
+  un.h0 = un.g * p.G + 2 * pr;
+  un.nact = (2 * pr + 1 < p.G) ? 2 : 1;
+  const int last = min(un.t * kRows + kRows - 1, p.N - 1);
+  un.nt = p.causal ? last / T + 1 : (p.N - 1) / T + 1;
+  return un;
+}
+
+struct Bars {
+  uint64_t* q_full;
+  uint64_t* q_empty;
+  uint64_t* k_full;
+  uint64_t* k_empty;
+  uint64_t* v_full;
+  uint64_t* v_empty;
+  uint64_t* s_full;  // [2]
+  uint64_t* p_full;  // [2]
+  uint64_t* o_done;  // [2]
+  uint64_t* o_free;  // [2]
+  uint64_t* drain;
+};
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void raise_abort(const Params& p, volatile int* abort_flag) {
+  if (!*abort_flag) {
+    *abort_flag = 1;
+    atomicOr(p.status, DEV_TIMEOUT);
+  }
+}
+
+// Warp-uniform wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
+                                          volatile int* abort_flag) {
+  uint32_t ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, p.wait_ns, abort_flag) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+template <int D, int T>
+__device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                         uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
+  using C = Cfg<D, T>;
+  uint32_t it = 0, kc = 0, vc = 0;  // tiles walked, K and V loads issued
+  int uc = 0;
+  bool ok = true;
+  bool q_issued = false;
+  uint32_t q_par = 0;
+  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+    const Unit un = decode_unit<T>(p, u);
+    if (!wait_or_abort(br.q_empty, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
+    mbar_arrive_expect_tx(br.q_full, un.nact * C::QB);
+    tma_load_3d(sQ, tq, br.q_full, 0, un.t * kRows, un.b * p.Hq + un.h0);
+    if (un.nact == 2) tma_load_3d(sQ + C::QB, tq, br.q_full, 0, un.t * kRows, un.b * p.Hq + un.h0 + 1);
+    q_issued = true;
+    q_par = uc & 1;
+    const int zkv = un.b * p.Hkv + un.g;
+    for (int k = 0; k < un.nt; ++k, ++it) {
+      const int jt = p.reverse ? un.nt - 1 - k : k;
+      const int s = int(it % C::NS);
+      const uint32_t ph = (it / C::NS) & 1u;
+      if (!wait_or_abort(br.k_empty + s, ph ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(br.k_full + s, C::KB);
+      tma_load_3d(sK + size_t(s) * C::KB, tk, br.k_full + s, 0, jt * T, zkv);
+      ++kc;
+      if (!wait_or_abort(br.v_empty + s, ph ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(br.v_full + s, C::VB);
+      tma_load_3d(sV + size_t(s) * C::VB, tv, br.v_full + s, jt * T, 0, zkv);
+      ++vc;
+    }
+  }
+  if (!ok) {
+    raise_abort(p, abort_flag);
+    // Drain: wait for every load still in flight (its barrier phase completes
+    // when the bytes land), bounded by the same limit.
+    const uint64_t limit = p.wait_ns;
+    volatile int no_abort = 0;
+    if (q_issued) wait_or_abort(br.q_full, q_par, limit, &no_abort);
+    for (uint32_t x = 0; x < uint32_t(C::NS); ++x) {
+      if (x < kc) {
+        const uint32_t last = kc - 1 - x;
+        wait_or_abort(br.k_full + last % C::NS, (last / C::NS) & 1u, limit, &no_abort);
+      }
+      if (x < vc) {
+        const uint32_t last = vc - 1 - x;
+        wait_or_abort(br.v_full + last % C::NS, (last / C::NS) & 1u, limit, &no_abort);
+      }
+    }
+  }
+}
+
+template <int D, int T>
+__device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br,
+                           volatile int* abort_flag) {
+  using C = Cfg<D, T>;
+  constexpr uint32_t idS = idesc_e4m3_f32(kRows, T);
+  constexpr uint32_t idO = idesc_e4m3_f32(kRows, D);
+  const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+  uint32_t it = 0;
+  int uc = 0;
+  uint32_t pc[2] = {0u, 0u};
+  bool ok = true;
+  bool issued_any = false;
+
+  auto issue_S = [&](int w, int s) {
+#pragma unroll
+    for (int kk = 0; kk < D / 32; ++kk) {
+      const uint64_t da = smem_desc(aQ + uint32_t(w * C::QB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
+      const uint64_t db = smem_desc(aK + uint32_t(s * C::KB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
+      mma_f8_ss(tmem + uint32_t(w * T), da, db, idS, kk > 0 ? 1u : 0u);
+    }
+  };
+  auto issue_PV = [&](int w, int s, bool acc) {
+#pragma unroll
+    for (int kk = 0; kk < T / 32; ++kk) {
+      const uint64_t db = smem_desc(aV + uint32_t(s * C::VB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
+      mma_f8_ts(tmem + uint32_t(2 * T + w * D), tmem + uint32_t(w * T + 8 * kk), db, idO,
+                (acc || kk > 0) ? 1u : 0u);
+    }
+  };
+
+  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+    const Unit un = decode_unit<T>(p, u);
+    if (!wait_or_abort(br.q_full, uc & 1, p.wait_ns, abort_flag)) { ok = false; break; }
+    tc_fence_after();
+    {
+      const int s = int(it % C::NS);
+      const uint32_t ph = (it / C::NS) & 1u;
+      if (!wait_or_abort(br.k_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      for (int w = 0; w < un.nact; ++w) {
+        issue_S(w, s);
+        mma_commit(br.s_full + w);
+      }
+      issued_any = true;
+      mma_commit(br.k_empty + s);
+      if (un.nt == 1) mma_commit(br.q_empty);
+    }
+    for (int k = 0; k < un.nt && ok; ++k) {
+      const uint32_t itk = it + uint32_t(k);
+      const int s = int(itk % C::NS);
+      const uint32_t ph = (itk / C::NS) & 1u;
+      if (!wait_or_abort(br.v_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      for (int w = 0; w < un.nact; ++w) {
+        if (k == 0 && !wait_or_abort(br.o_free + w, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
+        if (!wait_or_abort(br.p_full + w, pc[w] & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+        ++pc[w];
+        tc_fence_after();
+        issue_PV(w, s, k > 0);
+        mma_commit(br.o_done + w);
+        if (w == un.nact - 1) mma_commit(br.v_empty + s);
+        if (k + 1 < un.nt) {
+          const uint32_t it1 = itk + 1;
+          const int s1 = int(it1 % C::NS);
+          const uint32_t ph1 = (it1 / C::NS) & 1u;
+          if (w == 0) {
+            if (!wait_or_abort(br.k_full + s1, ph1, p.wait_ns, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+          }
+          issue_S(w, s1);
+          mma_commit(br.s_full + w);
+          if (w == un.nact - 1) {
+            mma_commit(br.k_empty + s1);
+            if (k + 1 == un.nt - 1) mma_commit(br.q_empty);
+          }
+        }
+      }
+    }
+    it += uint32_t(un.nt);
+  }
+  if (!ok) {
+    raise_abort(p, abort_flag);
+    if (issued_any) {
+      volatile int no_abort = 0;
+      mma_commit(br.drain);
+      wait_or_abort(br.drain, 0, p.wait_ns, &no_abort);
+    }
+  }
+}
+
+template <int D, int T, bool COUNT>
+__device__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br, volatile int* abort_flag) {
+  const int r = threadIdx.x & 127;           // row in the query tile = TMEM lane
+  const int wq = (threadIdx.x >> 5) & 3;     // warp within the warpgroup
+  const uint32_t lane_off = uint32_t(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_off + uint32_t(w * T);
+  const uint32_t tO = tmem + lane_off + uint32_t(2 * T + w * D);
+  uint32_t sc = 0, oc = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    const Unit un = decode_unit<T>(p, u);
+    if (w >= un.nact) {
+      mbar_arrive(br.o_free + w);
+      continue;
+    }
+    const int h = un.h0 + w;
+    const int bh = un.b * p.Hq + h, bg = un.b * p.Hkv + un.g;
+    const float c = __double2float_rn(
+        __dmul_rn(__dmul_rn(__dmul_rn(__dmul_rn(double(p.q_ds[bh]), double(p.k_ds[bg])), p.inv_sqrt_d), p.rot),
+                  p.log2e));
+    const int i = un.t * kRows + r;
+    float m = -INFINITY, l = 0.0f;
+    uint32_t uf0 = 0, uf1 = 0;
+    for (int k = 0; k < un.nt; ++k) {
+      const int jt = p.reverse ? un.nt - 1 - k : k;
+      const int j0 = jt * T;
+      if (!warp_wait(br.s_full + w, sc & 1u, p, abort_flag)) { ok = false; break; }
+      ++sc;
+      tc_fence_after();
+      float sv[T];
+#pragma unroll
+      for (int q = 0; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      float mt = -INFINITY;
+      const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
+      if (need_mask) {
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+          const int jj = j0 + j;
+          const bool vis = jj < p.N && (!p.causal || jj <= i);
+          sv[j] = vis ? __fmul_rn(sv[j], c) : -INFINITY;
+          mt = fmaxf(mt, sv[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+          sv[j] = __fmul_rn(sv[j], c);
+          mt = fmaxf(mt, sv[j]);
+        }
+      }
+      const float mnew = fmaxf(m, mt);
+      const float muse = (mnew == -INFINITY) ? 0.0f : mnew;
+      const float alpha = (mnew == -INFINITY) ? 1.0f : ex2(__fsub_rn(m, mnew));
+      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      uint32_t pk[T / 4];
+#pragma unroll
+      for (int q = 0; q < T / 4; ++q) {
+        float P[4], PS[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          P[e] = ex2(__fsub_rn(sv[4 * q + e], muse));
+          ls[e] = __fadd_rn(ls[e], P[e]);
+          PS[e] = __fmul_rn(P[e], p.S);
+        }
+        const uint32_t lo = cvt_e4m3x2(PS[0], PS[1]);
+        const uint32_t hi = cvt_e4m3x2(PS[2], PS[3]);
+        pk[q] = lo | (hi << 16);
+        if constexpr (COUNT) {
+          if (i < p.N) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int jj = j0 + 4 * q + e;
+              const uint32_t code = (pk[q] >> (8 * e)) & 0xFFu;
+              if (PS[e] > 0.0f && code == 0u && jj >= p.k_sink) {
+                if (jt == 0) ++uf0;
+                else ++uf1;
+              }
+            }
+          }
+        }
+      }
+      l = __fadd_rn(__fmul_rn(alpha, l), __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])));
+      if constexpr (T == 128) {
+        tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+      } else {
+        tmem_st8(tS, *reinterpret_cast<const uint32_t(*)[8]>(&pk[0]));
+        tmem_st8(tS + 8, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8]));
+      }
+      tmem_wait_st();
+      if (k > 0) {
+        // O_w must hold the previous tile's product before it is rescaled.
+        if (!warp_wait(br.o_done + w, oc & 1u, p, abort_flag)) { ok = false; break; }
+        ++oc;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tO + uint32_t(32 * q), o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
+            tmem_st32(tO + uint32_t(32 * q), o);
+          }
+          tmem_wait_st();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(br.p_full + w);
+      m = mnew;
+    }
+    if (!ok) break;
+    // epilogue: O = acc * dv / (S * l)
+    if (!warp_wait(br.o_done + w, oc & 1u, p, abort_flag)) { ok = false; break; }
+    ++oc;
+    tc_fence_after();
+    const float scale = __fdiv_rn(p.v_ds[bg], __fmul_rn(p.S, l));
+#pragma unroll 1
+    for (int q = 0; q < D / 32; ++q) {
+      uint32_t o[32];
+      tmem_ld32(tO + uint32_t(32 * q), o);
+      tmem_wait_ld();
+      reg_fence32(o);
+      if (i < p.N) {
+        const int64_t off = (int64_t(bh) * p.N + i) * D + 32 * q;
+        if (p.out_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + off);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(o[8 * v + 2 * e]), scale),
+                                                              __fmul_rn(__uint_as_float(o[8 * v + 2 * e + 1]), scale));
+              wv[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            dst[v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + off);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            dst[v] = make_float4(__fmul_rn(__uint_as_float(o[4 * v]), scale), __fmul_rn(__uint_as_float(o[4 * v + 1]), scale),
+                                 __fmul_rn(__uint_as_float(o[4 * v + 2]), scale), __fmul_rn(__uint_as_float(o[4 * v + 3]), scale));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(br.o_free + w);
+    if constexpr (COUNT) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        uf0 += __shfl_xor_sync(0xffffffffu, uf0, o);
+        uf1 += __shfl_xor_sync(0xffffffffu, uf1, o);
+      }
+      if ((threadIdx.x & 31) == 0) {
+        if (uf0) atomicAdd(p.uf + 2 * bh, (unsigned long long)uf0);
+        if (uf1) atomicAdd(p.uf + 2 * bh + 1, (unsigned long long)uf1);
+      }
+    }
+  }
+  if (!ok) raise_abort(p, abort_flag);
+}
+
+template <int D, int T, bool COUNT>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, const Params p) {
+  using C = Cfg<D, T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm;
+  uint8_t* sK = sQ + 2 * C::QB;
+  uint8_t* sV = sK + size_t(C::NS) * C::KB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + size_t(C::NS) * C::VB);
+  Bars br;
+  br.q_full = bars;
+  br.q_empty = bars + 1;
+  br.k_full = bars + 2;
+  br.k_empty = br.k_full + C::NS;
+  br.v_full = br.k_empty + C::NS;
+  br.v_empty = br.v_full + C::NS;
+  br.s_full = br.v_empty + C::NS;
+  br.p_full = br.s_full + 2;
+  br.o_done = br.p_full + 2;
+  br.o_free = br.o_done + 2;
+  br.drain = br.o_free + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(br.drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(br.q_full, 1);
+    mbar_init(br.q_empty, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(br.k_full + s, 1);
+      mbar_init(br.k_empty + s, 1);
+      mbar_init(br.v_full + s, 1);
+      mbar_init(br.v_empty + s, 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(br.s_full + w, 1);
+      mbar_init(br.p_full + w, 128);
+      mbar_init(br.o_done + w, 1);
+      mbar_init(br.o_free + w, 128);
+    }
+    mbar_init(br.drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_holder, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) mma_issuer<D, T>(p, tmem, sQ, sK, sV, br, abort_flag);
+  } else {
+    softmax_wg<D, T, COUNT>(p, warp >> 2, tmem, br, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, int T, bool COUNT>
+cudaError_t run(const FwdArgs& a, cudaStream_t st) {
+  using C = Cfg<D, T>;
+  CUtensorMap tq, tk, tv;
+  const CUtensorMapSwizzle swqk = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle swv = T == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (encode_tiled_3d(&tq, a.q8, D, a.N, uint64_t(a.B) * a.Hq, D, uint64_t(a.N) * D, D, kRows, swqk) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (encode_tiled_3d(&tk, a.k8, D, a.N, uint64_t(a.B) * a.Hkv, D, uint64_t(a.N) * D, D, T, swqk) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (encode_tiled_3d(&tv, a.v8t, uint64_t(a.ldv), D, uint64_t(a.B) * a.Hkv, uint64_t(a.ldv), uint64_t(a.ldv) * D, T,
+                      D, swv) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  Params p;
+  p.B = a.B;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.N = a.N;
+  p.G = a.Hq / a.Hkv;
+  p.pairs = (p.G + 1) / 2;
+  p.n_qt = (a.N + kRows - 1) / kRows;
+  p.n_units = p.n_qt * a.B * a.Hkv * p.pairs;
+  p.causal = a.causal;
+  p.reverse = a.reverse;
+  p.S = a.S;
+  p.q_ds = a.q_ds;
+  p.k_ds = a.k_ds;
+  p.v_ds = a.v_ds;
+  p.inv_sqrt_d = 1.0 / std::sqrt(double(D));
+  p.rot = a.rotate ? 1.0 / double(D) : 1.0;
+  p.log2e = 1.4426950408889634073599246810018921;
+  p.O = a.O;
+  p.out_bf16 = a.out_bf16;
+  p.uf = a.underflow;
+  p.k_sink = a.k_sink;
+  p.status = a.status;
+  p.wait_ns = a.wait_ns;
+  auto kern = k_attn_fwd<D, T, COUNT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+  if (e != cudaSuccess) return e;
+  const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
+  kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D, int T>
+cudaError_t run_count(const FwdArgs& a, cudaStream_t st) {
+  return a.underflow ? run<D, T, true>(a, st) : run<D, T, false>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 128) return a.T == 128 ? run_count<128, 128>(a, s) : run_count<128, 64>(a, s);
+  return a.T == 128 ? run_count<64, 128>(a, s) : run_count<64, 64>(a, s);
+}
+
+}  // namespace attnq

@@ -1,0 +1,64 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/attnq.h declares, and its host-only helpers behave as documented.
+No compute call is made here."""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+import synth
+
+
+@pytest.fixture(scope="module")
+def aq():
+    from precision_attention_numerics_gb300 import _build
+    _build.build()
+    import precision_attention_numerics_gb300 as aq
+    aq.load_library()
+    return aq
+
+
+def test_exports_every_declared_symbol(aq):
+    names = aq.exported_symbols()
+    assert {"attnq_prepare", "attnq_fwd", "attnq_fwd_ponly", "attnq_err", "attnq_device_status",
+            "attnq_status_string", "attnq_hadamard_signs", "attnq_version", "attnq_prepare_workspace",
+            "attnq_vt_ld"} <= set(names)
+    L = aq.load_library()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(aq):
+    assert aq.attnq_version() >= 100
+    for code, name in aq.STATUS.items():
+        assert aq.attnq_status_string(code).startswith(name)
+
+
+def test_vt_ld(aq):
+    assert [aq.attnq_vt_ld(n) for n in (0, 1, 15, 16, 17, 32768)] == [0, 16, 16, 16, 32, 32768]
+
+
+@pytest.mark.parametrize("seed", [0, 7, 123456789])
+def test_hadamard_signs_follow_splitmix64(aq, seed):
+    assert np.array_equal(aq.attnq_hadamard_signs(seed, 128), synth.hadamard_signs(seed, 128))
+
+
+def test_argument_checks_before_any_cuda_call(aq):
+    L = aq.load_library()
+    bad = [aq.AttnqDesc(1, 4, 3, 16, 64), aq.AttnqDesc(1, 1, 1, 16, 96), aq.AttnqDesc(0, 1, 1, 16, 64),
+           aq.AttnqDesc(1, 1, 1, 0, 64), aq.AttnqDesc(1, 1, 1, 16, 64, flags=64)]
+    want = [1, 2, 1, 1, 1]
+    for desc, code in zip(bad, want):
+        d = desc._c()
+        assert L.attnq_prepare_workspace(C.byref(d)) == 0
+        fake = C.c_void_p(4096)
+        rc = L.attnq_fwd(C.byref(d), fake, fake, fake, None, C.c_float(256.0), 0, 1, 128, fake, 0, None, 4, None)
+        assert rc == code, (desc, rc)
+
+
+def test_workspace_size_grows_with_centring(aq):
+    d0 = aq.AttnqDesc(2, 32, 8, 32768, 128, flags=aq.ATTNQ_VT_LAYOUT)
+    d1 = aq.AttnqDesc(2, 32, 8, 32768, 128, flags=aq.ATTNQ_VT_LAYOUT | aq.ATTNQ_CENTER_K)
+    w0, w1 = aq.attnq_prepare_workspace(d0), aq.attnq_prepare_workspace(d1)
+    assert 0 < w0 < w1
+    assert w1 - w0 >= 2 * 8 * (32768 // 128) * 128 * 4

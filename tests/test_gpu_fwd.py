@@ -1,0 +1,113 @@
+"""GPU parity of attnq_fwd (tcgen05 FP8 attention) against the oracle's
+kernel-faithful emulation run on the same E4M3 operands.
+
+Bars: per-head relative Frobenius difference <= 2e-3 (the exp2 and fp32
+accumulation orders differ, nothing else); underflow counts within 0.1% of
+the oracle's plus 2 absolute (a P*S within an ulp of the 2^-10 threshold can
+round either way under a different exp2)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(q, k, v, flags, S, order, causal, T, out_dtype=torch.float32, signs=None, k_sink=4):
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, oracle_bf16, rel_f
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    O, uf, st = gpu_fwd(desc, bufs, S, order, causal, T, out_dtype=out_dtype, k_sink=k_sink)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs)
+    B, Hq, N, d = q.shape
+    ref, uref = oracle.attn_quant(prep, (B, Hq, k.shape[1], N, d), flags, S, order, causal, T, k_sink=k_sink)
+    got = o_to_numpy(O).reshape(B * Hq, N, d)
+    if out_dtype == torch.bfloat16:
+        ref = oracle_bf16(ref)
+    assert np.all(np.isfinite(got))
+    r = rel_f(got, ref)
+    assert r.max() <= REL_F_TOL, r
+    tol = 0.001 * uref.astype(np.float64) + 2
+    assert np.all(np.abs(uf.astype(np.float64) - uref.astype(np.float64)) <= tol), (uf, uref)
+    return got, ref, uf, uref
+
+
+@pytest.mark.parametrize("S", [1.0, 256.0])
+def test_sink_probe_workload(S):
+    """Tiny sink probe: B=1, H=1, N=256, d=64, KV tile 64, delta=7, forward."""
+    q, k, v = synth.sink_inputs(1001, 1, 1, 256, 64, delta=7.0)
+    _, _, uf, uref = _run(q, k, v, 0, S, 0, True, 64)
+    if S == 1.0:
+        assert uref.sum() > 0 and uf.sum() > 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("T", [64, 128])
+@pytest.mark.parametrize("order", [0, 1])
+def test_shapes_and_orders(d, T, order):
+    q, k, v = synth.qwen_like_inputs(40 + d + T + order, 1, 4, 2, 384, d, key_norm=30.0, key_channels=4)
+    _run(q, k, v, 3, 256.0, order, True, T, signs=synth.hadamard_signs(3, d))
+
+
+@pytest.mark.parametrize("N", [1, 5, 17, 100, 129, 200, 255, 513])
+def test_ragged_lengths(N):
+    q, k, v = synth.sink_inputs(60 + N, 1, 2, N, 128, delta=5.0)
+    for T, order in ((128, 1), (64, 0)):
+        _run(q, k, v, 0, 256.0, order, True, T)
+
+
+@pytest.mark.parametrize("order", [0, 1])
+def test_non_causal(order):
+    q, k, v = synth.sink_inputs(77, 1, 2, 200, 64, delta=6.0)
+    _run(q, k, v, 0, 448.0, order, False, 64)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (3, 1), (7, 1), (6, 3), (8, 2)])
+def test_gqa_pairing(Hq, Hkv):
+    q, k, v = synth.qwen_like_inputs(80 + Hq, 2, Hq, Hkv, 260, 64, key_norm=30.0, key_channels=4)
+    _run(q, k, v, 2, 256.0, 1, True, 128)
+
+
+def test_bf16_output():
+    q, k, v = synth.qwen_like_inputs(90, 1, 4, 1, 300, 128, key_norm=40.0, key_channels=8)
+    _run(q, k, v, 3, 256.0, 1, True, 128, out_dtype=torch.bfloat16, signs=synth.hadamard_signs(4, 128))
+
+
+@pytest.mark.parametrize("S", [1.0, 256.0, 448.0])
+def test_pcollapse_counts_forward(S):
+    q, k, v = synth.sink_inputs(95, 1, 2, 1024, 128, delta=9.0)
+    _, _, uf, uref = _run(q, k, v, 0, S, 0, True, 128)
+
+
+def test_reverse_s256_no_late_underflow():
+    q, k, v = synth.sink_inputs(96, 1, 2, 1024, 128, delta=10.0)
+    _, _, uf, _ = _run(q, k, v, 0, 256.0, 1, True, 128)
+    assert uf[:, 1].sum() == 0
+
+
+def test_no_counters_same_output():
+    from tests.gpu_helpers import gpu_fwd, gpu_prepare
+    q, k, v = synth.sink_inputs(97, 1, 2, 300, 128, delta=7.0)
+    desc, bufs, _ = gpu_prepare(q, k, v, 0, None)
+    a, _, _ = gpu_fwd(desc, bufs, 256.0, 0, True, 128, count=True)
+    b, _, _ = gpu_fwd(desc, bufs, 256.0, 0, True, 128, count=False)
+    assert torch.equal(a, b)
+
+
+def test_rejects_bad_arguments():
+    import precision_attention_numerics_gb300 as aq
+    from tests.gpu_helpers import gpu_prepare
+    q, k, v = synth.sink_inputs(98, 1, 1, 64, 64, delta=1.0)
+    desc, bufs, _ = gpu_prepare(q, k, v, 0, None)
+    O = torch.empty((1, 1, 64, 64), device="cuda")
+    for kwargs, code in ((dict(S=0.0), 1), (dict(S=500.0), 1), (dict(S=float("nan")), 1), (dict(kv_tile=96), 2),
+                         (dict(kv_order=3), 1)):
+        args = dict(S=256.0, kv_order=0, causal=True, kv_tile=64)
+        args.update(kwargs)
+        with pytest.raises(aq.AttnqError) as e:
+            aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, args["S"], args["kv_order"], args["causal"],
+                         args["kv_tile"], O)
+        assert e.value.code == code
