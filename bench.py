@@ -1,0 +1,407 @@
+#!/usr/bin/env python
+"""Benchmark of the hot path on the long-context workload.
+
+One step = attnq_prepare (mean-key centring, random-sign Hadamard, per-head
+scales, E4M3 cast) + attnq_fwd (causal FP8 attention, reverse KV order,
+S = 256) over one batch: B=2, Hq=32, Hkv=8, N=32768, d=128, bf16 inputs,
+bf16 output.  The inputs (805 MB per step) exceed the 129 MB L2, so no flush
+is needed between steps.
+
+Prints one JSON line (rank 0).  `value` is algorithmic attention TFLOP/s
+(4*d per unmasked (i, j) pair, summed over all ranks) over the device-timed
+step; `e2e` repeats the measurement through the same C calls with the bf16
+inputs copied from pinned host memory and the output copied back inside the
+timed region.  Under torchrun every rank runs its own independent replica
+(weak scaling, no collective on the data path).
+
+--impl reference times the CPU oracle (the plain C++ implementation used by
+the tests) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal FP8 attention fwd TFLOP/s, % of GB300 FP8 peak; rel-Frobenius err vs FP64"
+WL = dict(B=2, Hq=32, Hkv=8, N=32768, d=128, kv_tile=128, S=256.0, kv_order="reverse")
+L2_BYTES = 129 * 1024 * 1024
+
+
+def attn_flops(B, Hq, N, d, rows=None):
+    """Algorithmic flops: 4*d per unmasked causal (i, j) pair."""
+    if rows is None:
+        pairs = N * (N + 1) // 2
+    else:
+        pairs = int(np.sum(np.asarray(rows, dtype=np.int64) + 1))
+    return 4.0 * d * pairs * B * Hq
+
+
+def prepare_bytes(B, Hq, Hkv, N, d, in_bytes=2):
+    """Algorithmic bytes of one prepare: read Q, K, V once, write their E4M3 codes once."""
+    elems = (B * Hq + 2 * B * Hkv) * N * d
+    return elems * in_bytes + elems
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def kernel_source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "precision_attention_numerics_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[2] == src_hash:
+                return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"attnq_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU) sample: the CPU baseline and the reference arm
+# ---------------------------------------------------------------------------
+
+def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0):
+    """Oracle prepare of one (batch, KV group) and quantised emulation of the
+    given query rows of its query heads.  Returns (seconds, flops, threads)."""
+    import oracle
+    G = WL["Hq"] // WL["Hkv"]
+    qs = q[b:b + 1, heads_group * G:(heads_group + 1) * G]
+    ks = k[b:b + 1, heads_group:heads_group + 1]
+    vs = v[b:b + 1, heads_group:heads_group + 1]
+    N, d = WL["N"], WL["d"]
+    t0 = time.perf_counter()
+    prep = oracle.prepare(qs, ks, vs, flags=oracle.ROTATE | oracle.CENTER_K, signs=signs)
+    oracle.attn_quant(prep, (1, G, 1, N, d), oracle.ROTATE | oracle.CENTER_K, WL["S"], 1, True, WL["kv_tile"],
+                      rows=rows)
+    dt = time.perf_counter() - t0
+    return dt, attn_flops(1, G, N, d, rows=rows), oracle.threads()
+
+
+def sample_rows(n_rows):
+    N = WL["N"]
+    return np.unique(np.linspace(N // 2, N - 1, n_rows).astype(np.int64))
+
+
+def make_inputs(seed):
+    import synth
+    return synth.long_context_inputs(seed, WL["B"], WL["Hq"], WL["Hkv"], WL["N"], WL["d"])
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import synth
+    q, k, v = make_inputs(5000)
+    signs = synth.hadamard_signs(17, WL["d"])
+    rows = sample_rows(args.ref_rows)
+    times, flops, thr = [], 0.0, 1
+    for s in range(args.warmup + args.steps):
+        dt, fl, thr = oracle_sample(q, k, v, signs, rows)
+        if s >= args.warmup:
+            times.append(dt)
+            flops = fl
+    mean = sum(times) / len(times)
+    value = flops / mean / 1e12
+    sample = (f"oracle prepare of one (batch, KV group) slice set (4 query heads, 1 KV head) + quantised "
+              f"emulation of {len(rows)} query rows in [N/2, N) of those 4 heads per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64/f32 emulation of e4m3", "data": "synthetic",
+            "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "step": "oracle sample (see cpu_baseline.sample)"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import precision_attention_numerics_gb300 as aq
+    import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    aq.load_library()
+    B, Hq, Hkv, N, d, T = WL["B"], WL["Hq"], WL["Hkv"], WL["N"], WL["d"], WL["kv_tile"]
+    S = WL["S"]
+    flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT
+    q_np, k_np, v_np = make_inputs(5000 + rank)
+    signs_np = synth.hadamard_signs(17, d)
+    dev = torch.device("cuda", local)
+    # pinned host copies (end-to-end leg) and device-resident inputs
+    Qh = torch.from_numpy(q_np).view(torch.bfloat16).pin_memory()
+    Kh = torch.from_numpy(k_np).view(torch.bfloat16).pin_memory()
+    Vh = torch.from_numpy(v_np).view(torch.bfloat16).pin_memory()
+    Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
+    signs = torch.from_numpy(signs_np).to(dev)
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, flags, signs)
+    bufs = aq.alloc_prepared(desc, device=dev)
+    O = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev)
+    Oh = torch.empty((B, Hq, N, d), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        aq.attnq_prepare(desc, Q, K, V, bufs.q8, bufs.k8, bufs.v8, bufs.scales, bufs.workspace)
+        aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, S, aq.ATTNQ_KV_REVERSE, True, T, O)
+
+    for _ in range(args.warmup):
+        step()
+    st = aq.attnq_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {aq.STATUS.get(st, st)} after warm-up")
+
+    # ---- device-resident timed region, with per-call events for the roofline
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for s in range(args.steps):
+            e0, e1, e2 = ev[s]
+            e0.record(stream)
+            aq.attnq_prepare(desc, Q, K, V, bufs.q8, bufs.k8, bufs.v8, bufs.scales, bufs.workspace)
+            e1.record(stream)
+            aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, S, aq.ATTNQ_KV_REVERSE, True, T, O)
+            e2.record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    elapsed = start.elapsed_time(end) / 1e3
+    t_prep = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / args.steps / 1e3
+    t_fwd = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / args.steps / 1e3
+    st = aq.attnq_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {aq.STATUS.get(st, st)} in the timed region")
+    if dist is not None:
+        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    # ---- end-to-end through the same C calls with host buffers
+    def e2e_step():
+        Q.copy_(Qh, non_blocking=True)
+        K.copy_(Kh, non_blocking=True)
+        V.copy_(Vh, non_blocking=True)
+        step()
+        Oh.copy_(O, non_blocking=True)
+
+    e2e_elapsed = float("nan")
+    if not args.no_e2e:
+        for _ in range(min(args.warmup, 2)):
+            e2e_step()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_elapsed = s0.elapsed_time(s1) / 1e3
+    if dist is not None and not args.no_e2e:
+        t = torch.tensor([e2e_elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_elapsed = float(t.item())
+    h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * 2
+    d2h = Oh.numel() * 2
+
+    flops_step = attn_flops(B, Hq, N, d)
+    value = flops_step * args.steps * world / elapsed / 1e12
+    e2e_value = flops_step * args.steps * world / e2e_elapsed / 1e12
+    peaks = load_peaks()
+    fp8_peak_sus = 2.0 * peaks["bf16_sus"]   # nominal fp8:bf16 dense ratio 4.5 : 2.25
+    fp8_peak_burst = 2.0 * peaks["bf16"]
+    fwd_tflops = flops_step / t_fwd / 1e12
+    prep_bytes = prepare_bytes(B, Hq, Hkv, N, d)
+    prep_gbs = prep_bytes / t_prep / 1e9
+    fwd_hash = kernel_source_hash(["attn_fwd.cu", "ptx.cuh"])
+    prep_hash = kernel_source_hash(["prepare.cu", "ptx.cuh"])
+
+    line = None
+    if rank == 0:
+        # per-head error against FP64 on a row sample (oracle, outside the timed region)
+        import oracle
+        rows = np.unique(np.array([0, 1, 127, 4095, N // 2 - 1, N // 2, N - 1], dtype=np.int64))
+        bh = sorted({0, B * Hq // 2 - 1, B * Hq // 2 + 5, B * Hq - 1})
+        Og = O.view(B * Hq, N, d)[bh][:, rows].float().cpu().numpy().astype(np.float64)
+        exact = oracle.attn_exact(q_np, k_np, v_np, bh_list=bh, rows=rows)
+        rel = np.linalg.norm(Og - exact, axis=(1, 2)) / np.linalg.norm(exact, axis=(1, 2))
+        err_sample = {"mean_log1p_relF": float(np.mean(np.log1p(rel))), "heads": bh,
+                      "rows": rows.tolist(), "reference": "oracle exact FP64 attention"}
+        cpu = None
+        if not args.no_cpu_baseline:
+            rows_s = sample_rows(args.cpu_rows)
+            dt, fl, thr = oracle_sample(q_np, k_np, v_np, signs_np, rows_s)
+            cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                   "sample": (f"oracle prepare of one (batch, KV group) (4 query heads, 1 KV head) + quantised "
+                              f"emulation of {len(rows_s)} query rows in [N/2, N) of those heads; "
+                              f"{dt:.1f} s of CPU time")}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "rotate": True, "center_k": True, "in_dtype": "bf16",
+                       "out_dtype": "bf16", "step": "attnq_prepare + attnq_fwd",
+                       "l2": "inputs 805 MB per step > 129 MB L2; no flush",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_fp8_peak": 100.0 * value / world / fp8_peak_sus,
+            "roofline": {"kernel": "attnq_fwd (k_attn_fwd<128,128>)", "bound": "tensor", "achieved": fwd_tflops,
+                         "peak": fp8_peak_sus, "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak_sus,
+                         "traffic": ncu_traffic("k_attn_fwd", fwd_hash),
+                         "peak_note": (f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 2 (nominal fp8:bf16);"
+                                       f" burst-based peak {fp8_peak_burst:.1f}"),
+                         "flops_per_launch": flops_step, "ms_per_launch": t_fwd * 1e3},
+            "roofline_prepare": {"kernel": "attnq_prepare (all passes)", "bound": "hbm", "achieved": prep_gbs,
+                                 "peak": peaks["hbm"], "unit": "GB/s", "frac": prep_gbs / peaks["hbm"],
+                                 "traffic": ncu_traffic("attnq_prepare", prep_hash),
+                                 "bytes_per_launch": prep_bytes, "ms_per_launch": t_prep * 1e3},
+            "err_vs_fp64": err_sample,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_elapsed / args.steps * 1e3},
+            "clocks": clocks,
+            "gpu_launches": args.steps * (7 if flags & aq.ATTNQ_CENTER_K else 5),
+        }
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--ref-rows", type=int, default=96)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--B", type=int, default=WL["B"], help="smaller batch for profiling captures")
+    ap.add_argument("--Hq", type=int, default=WL["Hq"])
+    ap.add_argument("--Hkv", type=int, default=WL["Hkv"])
+    args = ap.parse_args()
+    WL.update(B=args.B, Hq=args.Hq, Hkv=args.Hkv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

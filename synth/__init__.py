@@ -30,6 +30,7 @@ three books; these shapes stand in for them):
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 
@@ -54,29 +55,40 @@ def uniforms(seed: int, n: int) -> np.ndarray:
     return (splitmix64(seed, n) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
 
 
-def normals(seed: int, n: int, chunk: int = 1 << 24) -> np.ndarray:
+def _normals_block(seed: int, out: np.ndarray, pair0: int, m: int, n: int) -> None:
+    z = splitmix64(seed, 2 * m, offset=2 * pair0)
+    u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)  # (0, 1]
+    u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    del z
+    r = np.sqrt(-2.0 * np.log(u1))
+    th = (2.0 * math.pi) * u2
+    pair = np.empty(2 * m, dtype=np.float64)
+    pair[0::2] = r * np.cos(th)
+    pair[1::2] = r * np.sin(th)
+    lo = 2 * pair0
+    hi = min(n, lo + 2 * m)
+    out[lo:hi] = pair[: hi - lo]
+
+
+def normals(seed: int, n: int, chunk: int = 1 << 22, threads: int | None = None) -> np.ndarray:
     """n standard normals (float32) by Box-Muller on SplitMix64 pairs.
 
-    Generated in chunks so that large tensors do not need float64 copies of
-    the whole array.
+    Pair p uses stream outputs 2p+1 and 2p+2, so the result does not depend
+    on the chunking or the thread count; chunks run on a thread pool (numpy
+    releases the GIL inside its loops).
     """
     out = np.empty(n, dtype=np.float32)
     pairs_total = (n + 1) // 2
-    done = 0
-    while done < pairs_total:
-        m = min(chunk, pairs_total - done)
-        z = splitmix64(seed, 2 * m, offset=2 * done)
-        u1 = ((z[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * (2.0 ** -53)  # (0, 1]
-        u2 = (z[1::2] >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-        r = np.sqrt(-2.0 * np.log(u1))
-        th = (2.0 * math.pi) * u2
-        pair = np.empty(2 * m, dtype=np.float64)
-        pair[0::2] = r * np.cos(th)
-        pair[1::2] = r * np.sin(th)
-        lo = 2 * done
-        hi = min(n, lo + 2 * m)
-        out[lo:hi] = pair[: hi - lo]
-        done += m
+    starts = list(range(0, pairs_total, chunk))
+    if threads is None:
+        threads = min(16, os.cpu_count() or 1)
+    if len(starts) <= 1 or threads <= 1:
+        for p0 in starts:
+            _normals_block(seed, out, p0, min(chunk, pairs_total - p0), n)
+        return out
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda p0: _normals_block(seed, out, p0, min(chunk, pairs_total - p0), n), starts))
     return out
 
 
