@@ -368,8 +368,9 @@ def run_ours(args):
                                  "bytes_per_launch": prep_bytes, "ms_per_launch": t_prep * 1e3},
             "err_vs_fp64": err_sample,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_elapsed / args.steps * 1e3},
+            "e2e": None if args.no_e2e else {
+                "value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_elapsed / args.steps * 1e3},
             "clocks": clocks,
             "gpu_launches": args.steps * (7 if flags & aq.ATTNQ_CENTER_K else 5),
         }
