@@ -138,6 +138,27 @@ attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K,
                            cudaStream_t stream);
 
 /*
+ * attnq_prepare without a caller workspace.  The pages have no counterpart:
+ * this is a calling convention, not part of the method.  It is for callers
+ * that cannot allocate device memory when they call (for example a plugin
+ * hook of an inference runtime that must not allocate, or a process whose
+ * device memory is owned by another allocator).  The scratch lives in a fixed
+ * ATTNQ_STATIC_SCRATCH_BYTES array inside the library, which every GPU that
+ * loads the library holds until the process exits.  Arguments and results as
+ * attnq_prepare.  Returns ATTNQ_EUNSUPPORTED, before launching anything, when
+ * attnq_prepare_workspace(desc) exceeds ATTNQ_STATIC_SCRATCH_BYTES.  The
+ * first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  The call allocates nothing.  All calls share the one array and
+ * it keeps the last call's contents (each call clears what must start at
+ * zero): calls whose kernels overlap on the GPU - other streams, other host
+ * threads - race on it and must be serialised by the caller.
+ */
+#define ATTNQ_STATIC_SCRATCH_BYTES (4u << 20)
+attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const void* K, const void* V, uint8_t* q8,
+                                  uint8_t* k8, uint8_t* v8, const attnq_scales* out, cudaStream_t stream);
+
+/*
  * Causal FP8 attention forward [AN], [PC sec. 1]: for each query row i and
  * the KV tiles of width kv_tile (aligned at token 0) holding a key j <= i
  * (every key when causal == 0), visited forward (0 -> diagonal) or reverse

@@ -26,6 +26,8 @@ from .binding import (  # noqa: F401
     attnq_fwd_ponly,
     attnq_hadamard_signs,
     attnq_prepare,
+    attnq_prepare_static,
+    ATTNQ_STATIC_SCRATCH_BYTES,
     attnq_prepare_workspace,
     attnq_status_string,
     attnq_version,

@@ -100,6 +100,8 @@ def load_library():
     L.attnq_prepare_workspace.argtypes = [P]
     L.attnq_prepare.restype = i32
     L.attnq_prepare.argtypes = [P, P, P, P, P, P, P, P, P, sz, P]
+    L.attnq_prepare_static.restype = i32
+    L.attnq_prepare_static.argtypes = [P, P, P, P, P, P, P, P, P]
     L.attnq_fwd.restype = i32
     L.attnq_fwd.argtypes = [P, P, P, P, P, f32, i32, i32, i32, P, i32, P, i32, P]
     L.attnq_fwd_ponly.restype = i32
@@ -165,6 +167,17 @@ def attnq_prepare(desc: AttnqDesc, Q, K, V, q8, k8, v8, scales: AttnqScales, wor
     nbytes = workspace.numel() * workspace.element_size()
     _check(load_library().attnq_prepare(C.byref(d), _ptr(Q), _ptr(K), _ptr(V), _ptr(q8), _ptr(k8), _ptr(v8),
                                         C.byref(s), _ptr(workspace), nbytes, _stream(stream)), "attnq_prepare")
+
+
+def attnq_prepare_static(desc: AttnqDesc, Q, K, V, q8, k8, v8, scales: AttnqScales, stream=None) -> None:
+    """attnq_prepare with the library's fixed scratch array instead of a workspace
+    (for callers that cannot allocate; calls must not overlap on the GPU)."""
+    d, s = desc._c(), scales._c()
+    _check(load_library().attnq_prepare_static(C.byref(d), _ptr(Q), _ptr(K), _ptr(V), _ptr(q8), _ptr(k8), _ptr(v8),
+                                               C.byref(s), _stream(stream)), "attnq_prepare_static")
+
+
+ATTNQ_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 def attnq_fwd(desc: AttnqDesc, q8, k8, v8, scales: AttnqScales, S: float, kv_order: int, causal: bool,

@@ -175,6 +175,39 @@ attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K,
   return from_cuda(launch_prepare(a, stream));
 }
 
+attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const void* K, const void* V, uint8_t* q8,
+                                  uint8_t* k8, uint8_t* v8, const attnq_scales* out, cudaStream_t stream) {
+  static_assert(kStaticScratchBytes == ATTNQ_STATIC_SCRATCH_BYTES, "header and library disagree");
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (desc->in_dtype != ATTNQ_F32 && desc->in_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  if (!Q || !K || !V || !q8 || !k8 || !v8 || !out || !out->q_descale || !out->k_descale || !out->v_descale)
+    return ATTNQ_EINVAL;
+  if ((desc->flags & ATTNQ_ROTATE) && !desc->signs) return ATTNQ_EINVAL;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(q8) || !aligned16(k8) || !aligned16(v8))
+    return ATTNQ_EINVAL;
+  // larger problems need more scratch than the fixed array holds
+  if (attnq_prepare_workspace(desc) > kStaticScratchBytes) return ATTNQ_EUNSUPPORTED;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  void* scratch = nullptr;
+  if (static_scratch_address(&scratch) != cudaSuccess) return ATTNQ_ECUDA;
+  PrepareArgs a{};
+  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d;
+  a.bf16 = desc->in_dtype == ATTNQ_BF16;
+  a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
+  a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
+  a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
+  a.signs = desc->signs;
+  a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
+  a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
+  a.ldv = attnq_vt_ld(desc->N);
+  a.status = g_status_ptr[dev];
+  carve_prepare_workspace(a, scratch);   // the amax words are cleared by the launch itself
+  return from_cuda(launch_prepare(a, stream));
+}
+
 attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
                        const attnq_scales* scales, float S, int32_t kv_order, int32_t causal, int32_t kv_tile,
                        void* O, int32_t out_dtype, uint64_t* underflow_opt, int32_t k_sink, cudaStream_t stream) {

@@ -34,6 +34,10 @@ struct PrepareArgs {
 };
 
 size_t prepare_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int center);
+// Size of the fixed scratch array behind attnq_prepare_static (ATTNQ_STATIC_SCRATCH_BYTES).
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;
+// Device address of that array on the current device (looked up once per device).
+cudaError_t static_scratch_address(void** out);
 void carve_prepare_workspace(PrepareArgs& a, void* ws);
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t s);
 

@@ -12,6 +12,8 @@
 // covers two (d = 128) or four (d = 64) rows.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -333,6 +335,32 @@ void carve_prepare_workspace(PrepareArgs& a, void* ws) {
     a.mean_part = nullptr;
     a.mu = nullptr;
   }
+}
+
+// ---- fixed scratch for callers that cannot allocate -------------------------
+// attnq_prepare_static uses this file-scope array instead of a caller
+// workspace.  Every GPU that loads the library keeps it until the process
+// exits; all calls share it.  Its device address is looked up once per device
+// (host code must not pass the symbol itself to a kernel: on the host it is
+// only a stand-in).
+static __device__ __align__(256) unsigned char g_prepare_scratch[kStaticScratchBytes];
+
+cudaError_t static_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_prepare_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_prepare(const PrepareArgs& a, cudaStream_t s) {
