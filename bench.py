@@ -103,7 +103,7 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -144,6 +144,26 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """Largest x over all ranks (the slowest replica sets the job's time)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(flops_per_step: float, steps: int, world: int, elapsed_max: float) -> float:
+    """Whole-job TFLOP/s: every replica does the same work; the job ends with the slowest."""
+    return flops_per_step * steps * world / elapsed_max / 1e12
+
+
+def replica_seed(rank: int) -> int:
+    """Each replica draws its own batch (weak scaling: independent problems)."""
+    return 5000 + rank
 
 
 def dist_env():
@@ -232,7 +252,7 @@ def run_ours(args):
     B, Hq, Hkv, N, d, T = WL["B"], WL["Hq"], WL["Hkv"], WL["N"], WL["d"], WL["kv_tile"]
     S = WL["S"]
     flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT
-    q_np, k_np, v_np = make_inputs(5000 + rank)
+    q_np, k_np, v_np = make_inputs(replica_seed(rank))
     signs_np = synth.hadamard_signs(17, d)
     dev = torch.device("cuda", local)
     # pinned host copies (end-to-end leg) and device-resident inputs
@@ -282,10 +302,7 @@ def run_ours(args):
     st = aq.attnq_device_status()
     if st != 0:
         raise RuntimeError(f"device status {aq.STATUS.get(st, st)} in the timed region")
-    if dist is not None:
-        t = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, dist, dev)
 
     # ---- end-to-end through the same C calls with host buffers
     def e2e_step():
@@ -309,16 +326,14 @@ def run_ours(args):
         s1.record(stream)
         torch.cuda.synchronize()
         e2e_elapsed = s0.elapsed_time(s1) / 1e3
-    if dist is not None and not args.no_e2e:
-        t = torch.tensor([e2e_elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_elapsed = float(t.item())
+    if not args.no_e2e:
+        e2e_elapsed = max_over_ranks(e2e_elapsed, dist, dev)
     h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * 2
     d2h = Oh.numel() * 2
 
     flops_step = attn_flops(B, Hq, N, d)
-    value = flops_step * args.steps * world / elapsed / 1e12
-    e2e_value = flops_step * args.steps * world / e2e_elapsed / 1e12
+    value = replica_value(flops_step, args.steps, world, elapsed)
+    e2e_value = replica_value(flops_step, args.steps, world, e2e_elapsed)
     peaks = load_peaks()
     fp8_peak_sus = 2.0 * peaks["bf16_sus"]   # nominal fp8:bf16 dense ratio 4.5 : 2.25
     fp8_peak_burst = 2.0 * peaks["bf16"]
@@ -385,11 +400,11 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--B", type=int, default=WL["B"], help="smaller batch for profiling captures")

@@ -9,17 +9,23 @@
 //   O_acc = alpha*O_acc + sum_j p8_j v8_j;   O = O_acc * dv / (S * l).
 // The running maximum is exact; O is rescaled whenever alpha != 1 (a
 // skipped rescale with alpha == 1 is exact).
+// Arithmetic per score (two at a time with the packed f32x2 instructions):
+// the row maximum is taken on the raw q8.k8 sums (scaling by c > 0 commutes
+// with rounding and max), then P*S = 2^(fma(s, c, log2 S - m')) comes out of
+// one ex2, and the row sum accumulates P*S (= S*l, divided out at the end).
 //
 // Work unit: one 128-row query tile of two query heads that share a KV head
 // (GQA); both use the same K/V tiles and the same KV range.  A persistent
 // grid walks the units longest-first (query tiles nearest the end of the
 // sequence have the most KV tiles).
 //
-// CTA = 320 threads:
+// CTA = 384 threads:
 //   warps 0-3  softmax warpgroup 0 (query head h0), TMEM lanes 0..127 = rows
 //   warps 4-7  softmax warpgroup 1 (query head h0 + 1)
-//   warp 8     TMA producer: Q tiles once per unit, K and V^T tiles through
-//              an NS-stage ring
+//   warps 8-11 control warpgroup (warps 10 and 11 only wait at the end)
+//   warp 8     TMA producer: Q tiles once per unit (two buffers, so the next
+//              unit's Q loads during this one), K and V^T tiles through an
+//              NS-stage ring
 //   warp 9     TMEM allocator and MMA issuer (one thread)
 // TMEM columns: S_w at [w*T, w*T+T) (P_w overwrites its first T/4 columns as
 // packed E4M3, the A operand of the P.V MMA), O_w at [2T + w*D, 2T + w*D + D).
@@ -43,13 +49,18 @@ namespace attnq {
 namespace {
 
 constexpr int kRows = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;          // three warpgroups
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
+// Register split: launched at 168 per thread (384 x 168 = 64,512); the two
+// softmax warpgroups rise to 224, warpgroup 2 (producer, MMA, two idle warps)
+// drops to 56: 2 x 128 x 224 + 128 x 56 = 64,512.
+constexpr uint32_t kSoftmaxRegs = 224, kControlRegs = 56;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
 
 struct Params {
   int B, Hq, Hkv, N, G, pairs, n_qt, n_units;
   int causal, reverse;
-  float S;
+  float S, log2S;
   const float* q_ds;
   const float* k_ds;
   const float* v_ds;
@@ -67,7 +78,7 @@ struct Cfg {
   static constexpr int QB = kRows * D;  // bytes of one Q tile
   static constexpr int KB = T * D;      // bytes of one K stage
   static constexpr int VB = D * T;      // bytes of one V^T stage
-  static constexpr int NS0 = (196608 - 2 * QB) / (KB + VB);
+  static constexpr int NS0 = (230400 - 4 * QB) / (KB + VB);
   static constexpr int NS = NS0 > 6 ? 6 : NS0;
   static constexpr int COLS_USED = 2 * T + 2 * D;
   static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256u : 512u;
@@ -75,9 +86,10 @@ struct Cfg {
   static constexpr uint32_t SBO_QK = 8u * D;
   static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;
   static constexpr uint32_t SBO_V = 8u * T;
-  static constexpr int NBARS = 2 + 4 * NS + 8 + 1;
-  static constexpr size_t SMEM = 1024 + 2 * size_t(QB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
+  static constexpr int NBARS = 4 + 4 * NS + 8 + 1;
+  static constexpr size_t SMEM = 1024 + 4 * size_t(QB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
   static_assert(COLS_USED <= 512, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 struct Unit {
@@ -102,8 +114,8 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
 }
 
 struct Bars {
-  uint64_t* q_full;
-  uint64_t* q_empty;
+  uint64_t* q_full;   // [2] (Q buffer)
+  uint64_t* q_empty;  // [2]
   uint64_t* k_full;
   uint64_t* k_empty;
   uint64_t* v_full;
@@ -116,16 +128,16 @@ struct Bars {
 };
 
 // Bounded wait that also gives up when another role has aborted.
+// The thread sleeps inside try_wait (up to 20 us per try) instead of
+// spinning, so waiting warps take few issue slots from the softmax warps.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                               volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -146,22 +158,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 template <int D, int T>
-__device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+__device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                          uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
   using C = Cfg<D, T>;
   uint32_t it = 0, kc = 0, vc = 0;  // tiles walked, K and V loads issued
   int uc = 0;
   bool ok = true;
   bool q_issued = false;
-  uint32_t q_par = 0;
+  int q_last = 0;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
     const Unit un = decode_unit<T>(p, u);
-    if (!wait_or_abort(br.q_empty, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
-    mbar_arrive_expect_tx(br.q_full, un.nact * C::QB);
-    tma_load_3d(sQ, tq, br.q_full, 0, un.t * kRows, un.b * p.Hq + un.h0);
-    if (un.nact == 2) tma_load_3d(sQ + C::QB, tq, br.q_full, 0, un.t * kRows, un.b * p.Hq + un.h0 + 1);
+    const int qb = uc & 1;
+    if (!wait_or_abort(br.q_empty + qb, ((uc >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
+    uint8_t* q_dst = sQ + size_t(qb) * 2 * C::QB;
+    mbar_arrive_expect_tx(br.q_full + qb, un.nact * C::QB);
+    tma_load_3d(q_dst, tq, br.q_full + qb, 0, un.t * kRows, un.b * p.Hq + un.h0);
+    if (un.nact == 2) tma_load_3d(q_dst + C::QB, tq, br.q_full + qb, 0, un.t * kRows, un.b * p.Hq + un.h0 + 1);
     q_issued = true;
-    q_par = uc & 1;
+    q_last = uc;
     const int zkv = un.b * p.Hkv + un.g;
     for (int k = 0; k < un.nt; ++k, ++it) {
       const int jt = p.reverse ? un.nt - 1 - k : k;
@@ -183,7 +197,11 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
     // when the bytes land), bounded by the same limit.
     const uint64_t limit = p.wait_ns;
     volatile int no_abort = 0;
-    if (q_issued) wait_or_abort(br.q_full, q_par, limit, &no_abort);
+    if (q_issued) {
+      // the last two Q loads may still be in flight
+      for (int x = q_last; x >= 0 && x >= q_last - 1; --x)
+        wait_or_abort(br.q_full + (x & 1), (x >> 1) & 1, limit, &no_abort);
+    }
     for (uint32_t x = 0; x < uint32_t(C::NS); ++x) {
       if (x < kc) {
         const uint32_t last = kc - 1 - x;
@@ -198,7 +216,7 @@ __device__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorM
 }
 
 template <int D, int T>
-__device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br,
+__device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br,
                            volatile int* abort_flag) {
   using C = Cfg<D, T>;
   constexpr uint32_t idS = idesc_e4m3_f32(kRows, T);
@@ -210,10 +228,10 @@ __device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t*
   bool ok = true;
   bool issued_any = false;
 
-  auto issue_S = [&](int w, int s) {
+  auto issue_S = [&](int w, int s, int qb) {
 #pragma unroll
     for (int kk = 0; kk < D / 32; ++kk) {
-      const uint64_t da = smem_desc(aQ + uint32_t(w * C::QB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
+      const uint64_t da = smem_desc(aQ + uint32_t((2 * qb + w) * C::QB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
       const uint64_t db = smem_desc(aK + uint32_t(s * C::KB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
       mma_f8_ss(tmem + uint32_t(w * T), da, db, idS, kk > 0 ? 1u : 0u);
     }
@@ -229,7 +247,8 @@ __device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t*
 
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
     const Unit un = decode_unit<T>(p, u);
-    if (!wait_or_abort(br.q_full, uc & 1, p.wait_ns, abort_flag)) { ok = false; break; }
+    const int qb = uc & 1;
+    if (!wait_or_abort(br.q_full + qb, (uc >> 1) & 1, p.wait_ns, abort_flag)) { ok = false; break; }
     tc_fence_after();
     {
       const int s = int(it % C::NS);
@@ -237,12 +256,12 @@ __device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t*
       if (!wait_or_abort(br.k_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
       tc_fence_after();
       for (int w = 0; w < un.nact; ++w) {
-        issue_S(w, s);
+        issue_S(w, s, qb);
         mma_commit(br.s_full + w);
       }
       issued_any = true;
       mma_commit(br.k_empty + s);
-      if (un.nt == 1) mma_commit(br.q_empty);
+      if (un.nt == 1) mma_commit(br.q_empty + qb);
     }
     for (int k = 0; k < un.nt && ok; ++k) {
       const uint32_t itk = it + uint32_t(k);
@@ -266,11 +285,11 @@ __device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t*
             if (!wait_or_abort(br.k_full + s1, ph1, p.wait_ns, abort_flag)) { ok = false; break; }
             tc_fence_after();
           }
-          issue_S(w, s1);
+          issue_S(w, s1, qb);
           mma_commit(br.s_full + w);
           if (w == un.nact - 1) {
             mma_commit(br.k_empty + s1);
-            if (k + 1 == un.nt - 1) mma_commit(br.q_empty);
+            if (k + 1 == un.nt - 1) mma_commit(br.q_empty + qb);
           }
         }
       }
@@ -288,7 +307,7 @@ __device__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t*
 }
 
 template <int D, int T, bool COUNT>
-__device__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br, volatile int* abort_flag) {
+__device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br, volatile int* abort_flag) {
   const int r = threadIdx.x & 127;           // row in the query tile = TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;     // warp within the warpgroup
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
@@ -316,67 +335,93 @@ __device__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br
       if (!warp_wait(br.s_full + w, sc & 1u, p, abort_flag)) { ok = false; break; }
       ++sc;
       tc_fence_after();
-      float sv[T];
-#pragma unroll
-      for (int q = 0; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
-      tmem_wait_ld();
-#pragma unroll
-      for (int q = 0; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
-      float mt = -INFINITY;
+      // Two passes over S in TMEM, 64 columns at a time (keeps 64 scores live):
+      // pass 1 takes the row max of the raw sums (fl32(s * c) is monotone in s
+      // for c > 0, so max then scale equals scale then max); pass 2 forms
+      // P*S = 2^(fma(s, c, log2 S - m')), its row sum and the E4M3 codes, and
+      // stores the codes over the first T/4 columns of S (already read).
+      constexpr int H = T / 64;
       const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
-      if (need_mask) {
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < T; ++j) {
-          const int jj = j0 + j;
-          const bool vis = jj < p.N && (!p.causal || jj <= i);
-          sv[j] = vis ? __fmul_rn(sv[j], c) : -INFINITY;
-          mt = fmaxf(mt, sv[j]);
+      for (int hh = 0; hh < H; ++hh) {
+        float sv[64];
+        tmem_ld32f(tS + uint32_t(64 * hh), *reinterpret_cast<float(*)[32]>(&sv[0]));
+        tmem_ld32f(tS + uint32_t(64 * hh + 32), *reinterpret_cast<float(*)[32]>(&sv[32]));
+        tmem_wait_ld();
+        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[0]));
+        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32]));
+        if (need_mask) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int jj = j0 + 64 * hh + j;
+            const bool vis = jj < p.N && (!p.causal || jj <= i);
+            sv[j] = vis ? sv[j] : -INFINITY;
+          }
         }
-      } else {
 #pragma unroll
-        for (int j = 0; j < T; ++j) {
-          sv[j] = __fmul_rn(sv[j], c);
-          mt = fmaxf(mt, sv[j]);
+        for (int j = 0; j < 64; j += 8) {
+          mx[0] = fmax3(mx[0], sv[j], sv[j + 1]);
+          mx[1] = fmax3(mx[1], sv[j + 2], sv[j + 3]);
+          mx[2] = fmax3(mx[2], sv[j + 4], sv[j + 5]);
+          mx[3] = fmax3(mx[3], sv[j + 6], sv[j + 7]);
         }
       }
+      const float smax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      const float mt = (smax == -INFINITY) ? -INFINITY : __fmul_rn(smax, c);
       const float mnew = fmaxf(m, mt);
       const float muse = (mnew == -INFINITY) ? 0.0f : mnew;
       const float alpha = (mnew == -INFINITY) ? 1.0f : ex2(__fsub_rn(m, mnew));
-      float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      uint32_t pk[T / 4];
+      const float off = __fsub_rn(p.log2S, muse);
+      const uint64_t c2 = pack2(c, c), off2 = pack2(off, off);
+      uint64_t ls2[2] = {pack2(0.0f, 0.0f), pack2(0.0f, 0.0f)};
 #pragma unroll
-      for (int q = 0; q < T / 4; ++q) {
-        float P[4], PS[4];
+      for (int hh = 0; hh < H; ++hh) {
+        float sv[64];
+        tmem_ld32f(tS + uint32_t(64 * hh), *reinterpret_cast<float(*)[32]>(&sv[0]));
+        tmem_ld32f(tS + uint32_t(64 * hh + 32), *reinterpret_cast<float(*)[32]>(&sv[32]));
+        tmem_wait_ld();
+        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[0]));
+        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32]));
+        if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          P[e] = ex2(__fsub_rn(sv[4 * q + e], muse));
-          ls[e] = __fadd_rn(ls[e], P[e]);
-          PS[e] = __fmul_rn(P[e], p.S);
+          for (int j = 0; j < 64; ++j) {
+            const int jj = j0 + 64 * hh + j;
+            const bool vis = jj < p.N && (!p.causal || jj <= i);
+            sv[j] = vis ? sv[j] : -INFINITY;
+          }
         }
-        const uint32_t lo = cvt_e4m3x2(PS[0], PS[1]);
-        const uint32_t hi = cvt_e4m3x2(PS[2], PS[3]);
-        pk[q] = lo | (hi << 16);
-        if constexpr (COUNT) {
-          if (i < p.N) {
+        uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int jj = j0 + 4 * q + e;
-              const uint32_t code = (pk[q] >> (8 * e)) & 0xFFu;
-              if (PS[e] > 0.0f && code == 0u && jj >= p.k_sink) {
-                if (jt == 0) ++uf0;
-                else ++uf1;
+        for (int q = 0; q < 16; ++q) {
+          float PS[4];
+          unpack2(ffma2(pack2(sv[4 * q], sv[4 * q + 1]), c2, off2), PS[0], PS[1]);
+          unpack2(ffma2(pack2(sv[4 * q + 2], sv[4 * q + 3]), c2, off2), PS[2], PS[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) PS[e] = ex2(PS[e]);
+          ls2[0] = fadd2(ls2[0], pack2(PS[0], PS[1]));
+          ls2[1] = fadd2(ls2[1], pack2(PS[2], PS[3]));
+          pk[q] = pack_b16x2(cvt_e4m3x2(PS[0], PS[1]), cvt_e4m3x2(PS[2], PS[3]));
+          if constexpr (COUNT) {
+            if (i < p.N) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int jj = j0 + 64 * hh + 4 * q + e;
+                const uint32_t code = (pk[q] >> (8 * e)) & 0xFFu;
+                if (PS[e] > 0.0f && code == 0u && jj >= p.k_sink) {
+                  if (jt == 0) ++uf0;
+                  else ++uf1;
+                }
               }
             }
           }
         }
+        tmem_st16(tS + uint32_t(16 * hh), pk);
       }
-      l = __fadd_rn(__fmul_rn(alpha, l), __fadd_rn(__fadd_rn(ls[0], ls[1]), __fadd_rn(ls[2], ls[3])));
-      if constexpr (T == 128) {
-        tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-      } else {
-        tmem_st8(tS, *reinterpret_cast<const uint32_t(*)[8]>(&pk[0]));
-        tmem_st8(tS + 8, *reinterpret_cast<const uint32_t(*)[8]>(&pk[8]));
-      }
+      float la, lb, lc, ld;
+      unpack2(ls2[0], la, lb);
+      unpack2(ls2[1], lc, ld);
+      l = __fadd_rn(__fmul_rn(alpha, l), __fadd_rn(__fadd_rn(la, lb), __fadd_rn(lc, ld)));
       tmem_wait_st();
       if (k > 0) {
         // O_w must hold the previous tile's product before it is rescaled.
@@ -390,8 +435,14 @@ __device__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br
             tmem_ld32(tO + uint32_t(32 * q), o);
             tmem_wait_ld();
             reg_fence32(o);
+            const uint64_t a2 = pack2(alpha, alpha);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
+            for (int e = 0; e < 32; e += 2) {
+              float x0, x1;
+              unpack2(fmul2(pack2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), x0, x1);
+              o[e] = __float_as_uint(x0);
+              o[e + 1] = __float_as_uint(x1);
+            }
             tmem_st32(tO + uint32_t(32 * q), o);
           }
           tmem_wait_st();
@@ -402,11 +453,11 @@ __device__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br
       m = mnew;
     }
     if (!ok) break;
-    // epilogue: O = acc * dv / (S * l)
+    // epilogue: O = acc * dv / (S * l); the running sum already holds S * l
     if (!warp_wait(br.o_done + w, oc & 1u, p, abort_flag)) { ok = false; break; }
     ++oc;
     tc_fence_after();
-    const float scale = __fdiv_rn(p.v_ds[bg], __fmul_rn(p.S, l));
+    const float scale = __fdiv_rn(p.v_ds[bg], l);
 #pragma unroll 1
     for (int q = 0; q < D / 32; ++q) {
       uint32_t o[32];
@@ -462,14 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D, T>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm;
-  uint8_t* sK = sQ + 2 * C::QB;
+  uint8_t* sQ = sm;                      // [Q buffer][warpgroup]
+  uint8_t* sK = sQ + 4 * C::QB;
   uint8_t* sV = sK + size_t(C::NS) * C::KB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + size_t(C::NS) * C::VB);
   Bars br;
   br.q_full = bars;
-  br.q_empty = bars + 1;
-  br.k_full = bars + 2;
+  br.q_empty = bars + 2;
+  br.k_full = bars + 4;
   br.k_empty = br.k_full + C::NS;
   br.v_full = br.k_empty + C::NS;
   br.v_empty = br.v_full + C::NS;
@@ -483,8 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(br.q_full, 1);
-    mbar_init(br.q_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(br.q_full + b, 1);
+      mbar_init(br.q_empty + b, 1);
+    }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(br.k_full + s, 1);
       mbar_init(br.k_empty + s, 1);
@@ -515,11 +568,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == kProducerWarp) {
-    if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer<D, T>(p, tmem, sQ, sK, sV, br, abort_flag);
+  if (warp >= 8) {
+    regs_decrease<kControlRegs>();
+    if (warp == kProducerWarp) {
+      if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) mma_issuer<D, T>(p, tmem, sQ, sK, sV, br, abort_flag);
+    }
   } else {
+    regs_increase<kSoftmaxRegs>();
     softmax_wg<D, T, COUNT>(p, warp >> 2, tmem, br, abort_flag);
   }
 
@@ -556,6 +613,7 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   p.causal = a.causal;
   p.reverse = a.reverse;
   p.S = a.S;
+  p.log2S = float(std::log2(double(a.S)));
   p.q_ds = a.q_ds;
   p.k_ds = a.k_ds;
   p.v_ds = a.v_ds;
