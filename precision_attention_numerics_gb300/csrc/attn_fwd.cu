@@ -27,13 +27,21 @@
 //              unit's Q loads during this one), K and V^T tiles through an
 //              NS-stage ring
 //   warp 9     TMEM allocator and MMA issuer (one thread)
-// TMEM columns: S_w at [w*T, w*T+T) (P_w overwrites its first T/4 columns as
-// packed E4M3, the A operand of the P.V MMA), O_w at [2T + w*D, 2T + w*D + D).
-// Per tile and warpgroup w the MMA thread issues S_w = Q_w K^T
-// (kind::f8f6f4, M=128, N=T, K=32 per instruction), the softmax warpgroup
-// turns S_w into P_w, then the MMA thread issues O_w += P_w V (A from TMEM,
-// M=128, N=D) followed at once by S_w for the next tile, so warpgroup 1's
-// softmax overlaps warpgroup 0's MMAs and the other way round.
+// TMEM columns: S_w at [w*T, w*T+T), O_w at [2T + w*D, 2T + w*D + D).
+// Shared memory: Q[2 buffers][2 warpgroups], P[2 warpgroups][2 buffers] (the
+// E4M3 probabilities, written by the softmax threads in the 128-byte (or
+// 64-byte) swizzled K-major layout the MMA reads; tile n of a warpgroup uses
+// buffer n % 2, whose previous reader, P.V of tile n-2, is known complete),
+// the K and V^T rings.
+//
+// Pipeline per warpgroup w and tile k:
+//   MMA   S_w(k) = Q_w K(k)^T  (kind::f8f6f4, M=128, N=T, K=32 per instruction)
+//   SM    load S_w(k) from TMEM, then signal "S read"      -> MMA issues S_w(k+1)
+//   SM    row max, alpha, P*S, E4M3 codes, row sum
+//   SM    wait O_w += P_w(k-1) V(k-1); rescale O_w if alpha != 1; write P_w(k)
+//         to shared memory; signal "P ready"               -> MMA issues O_w += P_w(k) V(k)
+// so S_w(k+1) and the P.V products run on the tensor core while the softmax
+// warps compute, and the softmax never waits for its own S(k+1) MMA.
 //
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // DEV_TIMEOUT, every role leaves its loop, outstanding TMA loads and MMAs are
@@ -56,6 +64,9 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9;
 // drops to 56: 2 x 128 x 224 + 128 x 56 = 64,512.
 constexpr uint32_t kSoftmaxRegs = 224, kControlRegs = 56;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
+// Bound for draining in-flight copies and MMAs after an abort (independent of
+// the wait limit, so an abort never leaves copies in flight).
+constexpr uint64_t kDrainNs = 1000000000ull;
 
 struct Params {
   int B, Hq, Hkv, N, G, pairs, n_qt, n_units;
@@ -76,20 +87,22 @@ struct Params {
 template <int D, int T>
 struct Cfg {
   static constexpr int QB = kRows * D;  // bytes of one Q tile
+  static constexpr int PB = kRows * T;  // bytes of one P tile
   static constexpr int KB = T * D;      // bytes of one K stage
   static constexpr int VB = D * T;      // bytes of one V^T stage
-  static constexpr int NS0 = (230400 - 4 * QB) / (KB + VB);
+  static constexpr int NS0 = (230400 - 4 * QB - 4 * PB) / (KB + VB);
   static constexpr int NS = NS0 > 6 ? 6 : NS0;
   static constexpr int COLS_USED = 2 * T + 2 * D;
   static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256u : 512u;
   static constexpr uint32_t LAYOUT_QK = D == 128 ? 2u : 4u;  // 128B / 64B swizzle
   static constexpr uint32_t SBO_QK = 8u * D;
-  static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;
+  static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;    // V^T and P rows are T bytes
   static constexpr uint32_t SBO_V = 8u * T;
-  static constexpr int NBARS = 4 + 4 * NS + 8 + 1;
-  static constexpr size_t SMEM = 1024 + 4 * size_t(QB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
+  static constexpr int NBARS = 4 + 4 * NS + 10 + 1;
+  static constexpr size_t SMEM = 1024 + 4 * size_t(QB) + 4 * size_t(PB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NS >= 2, "pipeline depth");
 };
 
 struct Unit {
@@ -120,10 +133,11 @@ struct Bars {
   uint64_t* k_empty;
   uint64_t* v_full;
   uint64_t* v_empty;
-  uint64_t* s_full;  // [2]
-  uint64_t* p_full;  // [2]
-  uint64_t* o_done;  // [2]
-  uint64_t* o_free;  // [2]
+  uint64_t* s_full;  // [2] S_w in TMEM (MMA commit)
+  uint64_t* s_free;  // [2] S_w read by its warpgroup (128 arrivals)
+  uint64_t* p_full;  // [2] P_w in shared memory and O_w rescaled (128 arrivals)
+  uint64_t* o_done;  // [2] O_w += P_w V complete (MMA commit)
+  uint64_t* o_free;  // [2] O_w read by the epilogue (128 arrivals)
   uint64_t* drain;
 };
 
@@ -195,7 +209,7 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
     raise_abort(p, abort_flag);
     // Drain: wait for every load still in flight (its barrier phase completes
     // when the bytes land), bounded by the same limit.
-    const uint64_t limit = p.wait_ns;
+    const uint64_t limit = kDrainNs;
     volatile int no_abort = 0;
     if (q_issued) {
       // the last two Q loads may still be in flight
@@ -216,33 +230,43 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
 }
 
 template <int D, int T>
-__device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br,
-                           volatile int* abort_flag) {
+__device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t* sP, uint8_t* sK,
+                                           uint8_t* sV, const Bars& br, volatile int* abort_flag) {
   using C = Cfg<D, T>;
   constexpr uint32_t idS = idesc_e4m3_f32(kRows, T);
   constexpr uint32_t idO = idesc_e4m3_f32(kRows, D);
-  const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+  const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aK = smem_u32(sK), aV = smem_u32(sV);
   uint32_t it = 0;
   int uc = 0;
+  uint32_t n_s[2] = {0u, 0u};  // S MMAs issued per warpgroup (over the whole kernel)
   uint32_t pc[2] = {0u, 0u};
   bool ok = true;
   bool issued_any = false;
 
-  auto issue_S = [&](int w, int s, int qb) {
+  // S_w = Q_w K^T into S_w's TMEM columns; the previous S_w must have been read.
+  auto issue_S = [&](int w, int s, int qb) -> bool {
+    if (n_s[w] > 0 && !wait_or_abort(br.s_free + w, (n_s[w] - 1) & 1u, p.wait_ns, abort_flag)) return false;
+    ++n_s[w];
+    tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < D / 32; ++kk) {
       const uint64_t da = smem_desc(aQ + uint32_t((2 * qb + w) * C::QB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
       const uint64_t db = smem_desc(aK + uint32_t(s * C::KB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
       mma_f8_ss(tmem + uint32_t(w * T), da, db, idS, kk > 0 ? 1u : 0u);
     }
+    mma_commit(br.s_full + w);
+    issued_any = true;
+    return true;
   };
-  auto issue_PV = [&](int w, int s, bool acc) {
+  // O_w (+)= P_w V, both operands from shared memory
+  auto issue_PV = [&](int w, int s, int pbuf, bool acc) {
 #pragma unroll
     for (int kk = 0; kk < T / 32; ++kk) {
+      const uint64_t da = smem_desc(aP + uint32_t((2 * w + pbuf) * C::PB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
       const uint64_t db = smem_desc(aV + uint32_t(s * C::VB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
-      mma_f8_ts(tmem + uint32_t(2 * T + w * D), tmem + uint32_t(w * T + 8 * kk), db, idO,
-                (acc || kk > 0) ? 1u : 0u);
+      mma_f8_ss(tmem + uint32_t(2 * T + w * D), da, db, idO, (acc || kk > 0) ? 1u : 0u);
     }
+    mma_commit(br.o_done + w);
   };
 
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
@@ -252,47 +276,40 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8
     tc_fence_after();
     {
       const int s = int(it % C::NS);
-      const uint32_t ph = (it / C::NS) & 1u;
-      if (!wait_or_abort(br.k_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (!wait_or_abort(br.k_full + s, (it / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      for (int w = 0; w < un.nact; ++w) {
-        issue_S(w, s, qb);
-        mma_commit(br.s_full + w);
-      }
-      issued_any = true;
+      for (int w = 0; w < un.nact && ok; ++w) ok = issue_S(w, s, qb);
+      if (!ok) break;
       mma_commit(br.k_empty + s);
       if (un.nt == 1) mma_commit(br.q_empty + qb);
     }
     for (int k = 0; k < un.nt && ok; ++k) {
       const uint32_t itk = it + uint32_t(k);
+      // S for the next tile as soon as each warpgroup has read its S
+      if (k + 1 < un.nt) {
+        const uint32_t it1 = itk + 1;
+        const int s1 = int(it1 % C::NS);
+        if (!wait_or_abort(br.k_full + s1, (it1 / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        for (int w = 0; w < un.nact && ok; ++w) ok = issue_S(w, s1, qb);
+        if (!ok) break;
+        mma_commit(br.k_empty + s1);
+        if (k + 1 == un.nt - 1) mma_commit(br.q_empty + qb);
+      }
+      // P.V for this tile
       const int s = int(itk % C::NS);
-      const uint32_t ph = (itk / C::NS) & 1u;
-      if (!wait_or_abort(br.v_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (!wait_or_abort(br.v_full + s, (itk / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       tc_fence_after();
       for (int w = 0; w < un.nact; ++w) {
         if (k == 0 && !wait_or_abort(br.o_free + w, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
         if (!wait_or_abort(br.p_full + w, pc[w] & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+        const int pbuf = int(pc[w] & 1u);
         ++pc[w];
         tc_fence_after();
-        issue_PV(w, s, k > 0);
-        mma_commit(br.o_done + w);
-        if (w == un.nact - 1) mma_commit(br.v_empty + s);
-        if (k + 1 < un.nt) {
-          const uint32_t it1 = itk + 1;
-          const int s1 = int(it1 % C::NS);
-          const uint32_t ph1 = (it1 / C::NS) & 1u;
-          if (w == 0) {
-            if (!wait_or_abort(br.k_full + s1, ph1, p.wait_ns, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-          }
-          issue_S(w, s1, qb);
-          mma_commit(br.s_full + w);
-          if (w == un.nact - 1) {
-            mma_commit(br.k_empty + s1);
-            if (k + 1 == un.nt - 1) mma_commit(br.q_empty + qb);
-          }
-        }
+        issue_PV(w, s, pbuf, k > 0);
       }
+      if (!ok) break;
+      mma_commit(br.v_empty + s);
     }
     it += uint32_t(un.nt);
   }
@@ -301,19 +318,34 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8
     if (issued_any) {
       volatile int no_abort = 0;
       mma_commit(br.drain);
-      wait_or_abort(br.drain, 0, p.wait_ns, &no_abort);
+      wait_or_abort(br.drain, 0, kDrainNs, &no_abort);
     }
   }
 }
 
+// Byte offset of 16-byte chunk c of row r in a K-major tile whose rows are T
+// bytes, in the swizzled layout TMA writes and the MMA reads (128-byte
+// swizzle for T = 128: 8-row groups of 1024 bytes, chunk c ^ (r % 8); 64-byte
+// swizzle for T = 64: 8-row groups of 512 bytes, chunk c ^ ((r % 8) / 2)).
+template <int T>
+__device__ __forceinline__ uint32_t p_tile_offset(int r, int c) {
+  if constexpr (T == 128) {
+    return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+  } else {
+    return uint32_t((r >> 3) * 512 + (r & 7) * 64 + ((c ^ ((r & 7) >> 1)) << 4));
+  }
+}
+
 template <int D, int T, bool COUNT>
-__device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem, const Bars& br, volatile int* abort_flag) {
+__device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem, uint8_t* sP, const Bars& br,
+                                           volatile int* abort_flag) {
   const int r = threadIdx.x & 127;           // row in the query tile = TMEM lane
   const int wq = (threadIdx.x >> 5) & 3;     // warp within the warpgroup
   const uint32_t lane_off = uint32_t(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + uint32_t(w * T);
   const uint32_t tO = tmem + lane_off + uint32_t(2 * T + w * D);
-  uint32_t sc = 0, oc = 0;
+  uint8_t* my_p = sP + size_t(2 * w) * kRows * T;
+  uint32_t sc = 0, oc = 0, np = 0;  // S tiles read, P.V products waited for, P tiles written
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = decode_unit<T>(p, u);
@@ -326,6 +358,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
     const float c = __double2float_rn(
         __dmul_rn(__dmul_rn(__dmul_rn(__dmul_rn(double(p.q_ds[bh]), double(p.k_ds[bg])), p.inv_sqrt_d), p.rot),
                   p.log2e));
+    const uint64_t c2 = pack2(c, c);
     const int i = un.t * kRows + r;
     float m = -INFINITY, l = 0.0f;
     uint32_t uf0 = 0, uf1 = 0;
@@ -335,65 +368,49 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       if (!warp_wait(br.s_full + w, sc & 1u, p, abort_flag)) { ok = false; break; }
       ++sc;
       tc_fence_after();
-      // Two passes over S in TMEM, 64 columns at a time (keeps 64 scores live):
-      // pass 1 takes the row max of the raw sums (fl32(s * c) is monotone in s
-      // for c > 0, so max then scale equals scale then max); pass 2 forms
-      // P*S = 2^(fma(s, c, log2 S - m')), its row sum and the E4M3 codes, and
-      // stores the codes over the first T/4 columns of S (already read).
-      constexpr int H = T / 64;
+      float sv[T];
+#pragma unroll
+      for (int q = 0; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      // S_w is in registers: the MMA thread may overwrite it with the next tile
+      tc_fence_before();
+      mbar_arrive(br.s_free + w);
       const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
+      if (need_mask) {
+        // keys j0 + j are visible for j < lim (causal: j0 + j <= i; always j0 + j < N)
+        const int lim = min(p.N - j0, p.causal ? i - j0 + 1 : T);
+#pragma unroll
+        for (int j = 0; j < T; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
+      }
+      // row max of the raw sums: fl32(s * c) is monotone in s for c > 0
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int hh = 0; hh < H; ++hh) {
-        float sv[64];
-        tmem_ld32f(tS + uint32_t(64 * hh), *reinterpret_cast<float(*)[32]>(&sv[0]));
-        tmem_ld32f(tS + uint32_t(64 * hh + 32), *reinterpret_cast<float(*)[32]>(&sv[32]));
-        tmem_wait_ld();
-        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[0]));
-        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32]));
-        if (need_mask) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int jj = j0 + 64 * hh + j;
-            const bool vis = jj < p.N && (!p.causal || jj <= i);
-            sv[j] = vis ? sv[j] : -INFINITY;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 64; j += 8) {
-          mx[0] = fmax3(mx[0], sv[j], sv[j + 1]);
-          mx[1] = fmax3(mx[1], sv[j + 2], sv[j + 3]);
-          mx[2] = fmax3(mx[2], sv[j + 4], sv[j + 5]);
-          mx[3] = fmax3(mx[3], sv[j + 6], sv[j + 7]);
-        }
+      for (int j = 0; j < T; j += 8) {
+        mx[0] = fmax3(mx[0], sv[j], sv[j + 1]);
+        mx[1] = fmax3(mx[1], sv[j + 2], sv[j + 3]);
+        mx[2] = fmax3(mx[2], sv[j + 4], sv[j + 5]);
+        mx[3] = fmax3(mx[3], sv[j + 6], sv[j + 7]);
       }
       const float smax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       const float mt = (smax == -INFINITY) ? -INFINITY : __fmul_rn(smax, c);
       const float mnew = fmaxf(m, mt);
       const float muse = (mnew == -INFINITY) ? 0.0f : mnew;
       const float alpha = (mnew == -INFINITY) ? 1.0f : ex2(__fsub_rn(m, mnew));
+      // P*S = 2^(s*c + (log2 S - m'))
       const float off = __fsub_rn(p.log2S, muse);
-      const uint64_t c2 = pack2(c, c), off2 = pack2(off, off);
+      const uint64_t off2 = pack2(off, off);
       uint64_t ls2[2] = {pack2(0.0f, 0.0f), pack2(0.0f, 0.0f)};
+      // codes go straight to P buffer np % 2 (its last reader, P.V of the tile
+      // before the previous one, completed before the previous tile's rescale)
+      uint8_t* pbuf = my_p + size_t(np & 1u) * kRows * T;
 #pragma unroll
-      for (int hh = 0; hh < H; ++hh) {
-        float sv[64];
-        tmem_ld32f(tS + uint32_t(64 * hh), *reinterpret_cast<float(*)[32]>(&sv[0]));
-        tmem_ld32f(tS + uint32_t(64 * hh + 32), *reinterpret_cast<float(*)[32]>(&sv[32]));
-        tmem_wait_ld();
-        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[0]));
-        reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32]));
-        if (need_mask) {
+      for (int cch = 0; cch < T / 16; ++cch) {
+        uint32_t pw[4];
 #pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int jj = j0 + 64 * hh + j;
-            const bool vis = jj < p.N && (!p.causal || jj <= i);
-            sv[j] = vis ? sv[j] : -INFINITY;
-          }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int qq = 0; qq < 4; ++qq) {
+          const int q = 4 * cch + qq;
           float PS[4];
           unpack2(ffma2(pack2(sv[4 * q], sv[4 * q + 1]), c2, off2), PS[0], PS[1]);
           unpack2(ffma2(pack2(sv[4 * q + 2], sv[4 * q + 3]), c2, off2), PS[2], PS[3]);
@@ -401,13 +418,13 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
           for (int e = 0; e < 4; ++e) PS[e] = ex2(PS[e]);
           ls2[0] = fadd2(ls2[0], pack2(PS[0], PS[1]));
           ls2[1] = fadd2(ls2[1], pack2(PS[2], PS[3]));
-          pk[q] = pack_b16x2(cvt_e4m3x2(PS[0], PS[1]), cvt_e4m3x2(PS[2], PS[3]));
+          pw[qq] = pack_b16x2(cvt_e4m3x2(PS[0], PS[1]), cvt_e4m3x2(PS[2], PS[3]));
           if constexpr (COUNT) {
             if (i < p.N) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int jj = j0 + 64 * hh + 4 * q + e;
-                const uint32_t code = (pk[q] >> (8 * e)) & 0xFFu;
+                const int jj = j0 + 4 * q + e;
+                const uint32_t code = (pw[qq] >> (8 * e)) & 0xFFu;
                 if (PS[e] > 0.0f && code == 0u && jj >= p.k_sink) {
                   if (jt == 0) ++uf0;
                   else ++uf1;
@@ -416,38 +433,45 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
             }
           }
         }
-        tmem_st16(tS + uint32_t(16 * hh), pk);
+        *reinterpret_cast<uint4*>(pbuf + p_tile_offset<T>(r, cch)) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       }
+      ++np;
       float la, lb, lc, ld;
       unpack2(ls2[0], la, lb);
       unpack2(ls2[1], lc, ld);
       l = __fadd_rn(__fmul_rn(alpha, l), __fadd_rn(__fadd_rn(la, lb), __fadd_rn(lc, ld)));
-      tmem_wait_st();
       if (k > 0) {
-        // O_w must hold the previous tile's product before it is rescaled.
+        // O_w += P_w(k-1) V(k-1) must be complete before O_w is rescaled.
         if (!warp_wait(br.o_done + w, oc & 1u, p, abort_flag)) { ok = false; break; }
         ++oc;
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+          const uint64_t a2 = pack2(alpha, alpha);
 #pragma unroll 1
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld32(tO + uint32_t(32 * q), o);
+          for (int q = 0; q < D / 64; ++q) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tO + uint32_t(64 * q), o0);
+            tmem_ld32(tO + uint32_t(64 * q + 32), o1);
             tmem_wait_ld();
-            reg_fence32(o);
-            const uint64_t a2 = pack2(alpha, alpha);
+            reg_fence32(o0);
+            reg_fence32(o1);
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               float x0, x1;
-              unpack2(fmul2(pack2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), x0, x1);
-              o[e] = __float_as_uint(x0);
-              o[e + 1] = __float_as_uint(x1);
+              unpack2(fmul2(pack2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2), x0, x1);
+              o0[e] = __float_as_uint(x0);
+              o0[e + 1] = __float_as_uint(x1);
+              unpack2(fmul2(pack2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2), x0, x1);
+              o1[e] = __float_as_uint(x0);
+              o1[e + 1] = __float_as_uint(x1);
             }
-            tmem_st32(tO + uint32_t(32 * q), o);
+            tmem_st32(tO + uint32_t(64 * q), o0);
+            tmem_st32(tO + uint32_t(64 * q + 32), o1);
           }
           tmem_wait_st();
         }
       }
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(br.p_full + w);
       m = mnew;
@@ -514,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm;                      // [Q buffer][warpgroup]
-  uint8_t* sK = sQ + 4 * C::QB;
+  uint8_t* sP = sQ + 4 * C::QB;          // [warpgroup][P buffer]
+  uint8_t* sK = sP + 4 * C::PB;
   uint8_t* sV = sK + size_t(C::NS) * C::KB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + size_t(C::NS) * C::VB);
   Bars br;
@@ -525,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   br.v_full = br.k_empty + C::NS;
   br.v_empty = br.v_full + C::NS;
   br.s_full = br.v_empty + C::NS;
-  br.p_full = br.s_full + 2;
+  br.s_free = br.s_full + 2;
+  br.p_full = br.s_free + 2;
   br.o_done = br.p_full + 2;
   br.o_free = br.o_done + 2;
   br.drain = br.o_free + 2;
@@ -546,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(br.s_full + w, 1);
+      mbar_init(br.s_free + w, 128);
       mbar_init(br.p_full + w, 128);
       mbar_init(br.o_done + w, 1);
       mbar_init(br.o_free + w, 128);
@@ -573,11 +600,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
       if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_issuer<D, T>(p, tmem, sQ, sK, sV, br, abort_flag);
+      if (lane == 0) mma_issuer<D, T>(p, tmem, sQ, sP, sK, sV, br, abort_flag);
     }
   } else {
     regs_increase<kSoftmaxRegs>();
-    softmax_wg<D, T, COUNT>(p, warp >> 2, tmem, br, abort_flag);
+    softmax_wg<D, T, COUNT>(p, warp >> 2, tmem, sP, br, abort_flag);
   }
 
   tc_fence_before();
