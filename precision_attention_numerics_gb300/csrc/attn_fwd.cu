@@ -22,11 +22,13 @@
 // CTA = 384 threads:
 //   warps 0-3  softmax warpgroup 0 (query head h0), TMEM lanes 0..127 = rows
 //   warps 4-7  softmax warpgroup 1 (query head h0 + 1)
-//   warps 8-11 control warpgroup (warps 10 and 11 only wait at the end)
+//   warps 8-11 control warpgroup (warp 11 only waits at the end)
 //   warp 8     TMA producer: Q tiles once per unit (two buffers, so the next
 //              unit's Q loads during this one), K and V^T tiles through an
 //              NS-stage ring
-//   warp 9     TMEM allocator and MMA issuer (one thread)
+//   warp 9     TMEM allocator; lane 0 issues warpgroup 0's MMAs
+//   warp 10    lane 0 issues warpgroup 1's MMAs (each warpgroup's MMAs are
+//              in order; the two streams do not wait for each other)
 // TMEM columns: S_w at [w*T, w*T+T), O_w at [2T + w*D, 2T + w*D + D).
 // Shared memory: Q[2 buffers][2 warpgroups], P[2 warpgroups][2 buffers] (the
 // E4M3 probabilities, written by the softmax threads in the 128-byte (or
@@ -38,8 +40,12 @@
 //   MMA   S_w(k) = Q_w K(k)^T  (kind::f8f6f4, M=128, N=T, K=32 per instruction)
 //   SM    load S_w(k) from TMEM, then signal "S read"      -> MMA issues S_w(k+1)
 //   SM    row max, alpha, P*S, E4M3 codes, row sum
-//   SM    wait O_w += P_w(k-1) V(k-1); rescale O_w if alpha != 1; write P_w(k)
-//         to shared memory; signal "P ready"               -> MMA issues O_w += P_w(k) V(k)
+//   SM    write P_w(k) to shared memory; only if some row's alpha != 1, wait
+//         for O_w += P_w(k-1) V(k-1) and rescale O_w; signal "P ready"
+//                                                          -> MMA issues O_w += P_w(k) V(k)
+// P.V completions alternate between two barriers per warpgroup (product n
+// on barrier n % 2), so the softmax waits only for the products it needs:
+// product n-2 before reusing its P buffer, n-1 before a rescale.
 // so S_w(k+1) and the P.V products run on the tensor core while the softmax
 // warps compute, and the softmax never waits for its own S(k+1) MMA.
 //
@@ -58,7 +64,7 @@ namespace {
 
 constexpr int kRows = 128;
 constexpr int kThreads = 384;          // three warpgroups
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of warpgroups 0 and 1
 // Register split: launched at 168 per thread (384 x 168 = 64,512); the two
 // softmax warpgroups rise to 224, warpgroup 2 (producer, MMA, two idle warps)
 // drops to 56: 2 x 128 x 224 + 128 x 56 = 64,512.
@@ -98,7 +104,7 @@ struct Cfg {
   static constexpr uint32_t SBO_QK = 8u * D;
   static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;    // V^T and P rows are T bytes
   static constexpr uint32_t SBO_V = 8u * T;
-  static constexpr int NBARS = 4 + 4 * NS + 10 + 1;
+  static constexpr int NBARS = 4 + 4 * NS + 12 + 2;
   static constexpr size_t SMEM = 1024 + 4 * size_t(QB) + 4 * size_t(PB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -136,7 +142,7 @@ struct Bars {
   uint64_t* s_full;  // [2] S_w in TMEM (MMA commit)
   uint64_t* s_free;  // [2] S_w read by its warpgroup (128 arrivals)
   uint64_t* p_full;  // [2] P_w in shared memory and O_w rescaled (128 arrivals)
-  uint64_t* o_done;  // [2] O_w += P_w V complete (MMA commit)
+  uint64_t* o_done;  // [2][2] O_w += P_w V of product n complete, on [w][n % 2] (MMA commit)
   uint64_t* o_free;  // [2] O_w read by the epilogue (128 arrivals)
   uint64_t* drain;
 };
@@ -229,44 +235,38 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
   }
 }
 
+// Issues the MMAs of warpgroup w.  K/V stage and Q buffer barriers take one
+// arrival from each of the two issuing threads (a commit when the thread's
+// warpgroup used them, a plain arrive when it sat the unit out).
 template <int D, int T>
-__device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8_t* sQ, uint8_t* sP, uint8_t* sK,
-                                           uint8_t* sV, const Bars& br, volatile int* abort_flag) {
+__device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem, uint8_t* sQ, uint8_t* sP,
+                                           uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
   using C = Cfg<D, T>;
   constexpr uint32_t idS = idesc_e4m3_f32(kRows, T);
   constexpr uint32_t idO = idesc_e4m3_f32(kRows, D);
   const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aK = smem_u32(sK), aV = smem_u32(sV);
+  const uint32_t tS = tmem + uint32_t(w * T), tO = tmem + uint32_t(2 * T + w * D);
   uint32_t it = 0;
   int uc = 0;
-  uint32_t n_s[2] = {0u, 0u};  // S MMAs issued per warpgroup (over the whole kernel)
-  uint32_t pc[2] = {0u, 0u};
+  uint32_t n_s = 0;  // S MMAs issued (whole kernel)
+  uint32_t pc = 0;   // P.V products issued (whole kernel)
   bool ok = true;
   bool issued_any = false;
 
-  // S_w = Q_w K^T into S_w's TMEM columns; the previous S_w must have been read.
-  auto issue_S = [&](int w, int s, int qb) -> bool {
-    if (n_s[w] > 0 && !wait_or_abort(br.s_free + w, (n_s[w] - 1) & 1u, p.wait_ns, abort_flag)) return false;
-    ++n_s[w];
+  // S_w = Q_w K^T; the previous S_w must have been read by the warpgroup.
+  auto issue_S = [&](int s, int qb) -> bool {
+    if (n_s > 0 && !wait_or_abort(br.s_free + w, (n_s - 1) & 1u, p.wait_ns, abort_flag)) return false;
+    ++n_s;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < D / 32; ++kk) {
       const uint64_t da = smem_desc(aQ + uint32_t((2 * qb + w) * C::QB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
       const uint64_t db = smem_desc(aK + uint32_t(s * C::KB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
-      mma_f8_ss(tmem + uint32_t(w * T), da, db, idS, kk > 0 ? 1u : 0u);
+      mma_f8_ss(tS, da, db, idS, kk > 0 ? 1u : 0u);
     }
     mma_commit(br.s_full + w);
     issued_any = true;
     return true;
-  };
-  // O_w (+)= P_w V, both operands from shared memory
-  auto issue_PV = [&](int w, int s, int pbuf, bool acc) {
-#pragma unroll
-    for (int kk = 0; kk < T / 32; ++kk) {
-      const uint64_t da = smem_desc(aP + uint32_t((2 * w + pbuf) * C::PB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
-      const uint64_t db = smem_desc(aV + uint32_t(s * C::VB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
-      mma_f8_ss(tmem + uint32_t(2 * T + w * D), da, db, idO, (acc || kk > 0) ? 1u : 0u);
-    }
-    mma_commit(br.o_done + w);
   };
 
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
@@ -274,41 +274,54 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8
     const int qb = uc & 1;
     if (!wait_or_abort(br.q_full + qb, (uc >> 1) & 1, p.wait_ns, abort_flag)) { ok = false; break; }
     tc_fence_after();
+    if (w >= un.nact) {
+      // this warpgroup sits the unit out: release each stage and the Q buffer
+      for (int k = 0; k < un.nt && ok; ++k) {
+        const uint32_t itk = it + uint32_t(k);
+        const int s = int(itk % C::NS);
+        const uint32_t ph = (itk / C::NS) & 1u;
+        if (!wait_or_abort(br.k_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
+        mbar_arrive(br.k_empty + s);
+        if (!wait_or_abort(br.v_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
+        mbar_arrive(br.v_empty + s);
+      }
+      mbar_arrive(br.q_empty + qb);
+      it += uint32_t(un.nt);
+      continue;
+    }
     {
       const int s = int(it % C::NS);
       if (!wait_or_abort(br.k_full + s, (it / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      for (int w = 0; w < un.nact && ok; ++w) ok = issue_S(w, s, qb);
-      if (!ok) break;
+      if (!issue_S(s, qb)) { ok = false; break; }
       mma_commit(br.k_empty + s);
       if (un.nt == 1) mma_commit(br.q_empty + qb);
     }
     for (int k = 0; k < un.nt && ok; ++k) {
       const uint32_t itk = it + uint32_t(k);
-      // S for the next tile as soon as each warpgroup has read its S
       if (k + 1 < un.nt) {
         const uint32_t it1 = itk + 1;
         const int s1 = int(it1 % C::NS);
         if (!wait_or_abort(br.k_full + s1, (it1 / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        for (int w = 0; w < un.nact && ok; ++w) ok = issue_S(w, s1, qb);
-        if (!ok) break;
+        if (!issue_S(s1, qb)) { ok = false; break; }
         mma_commit(br.k_empty + s1);
         if (k + 1 == un.nt - 1) mma_commit(br.q_empty + qb);
       }
-      // P.V for this tile
       const int s = int(itk % C::NS);
       if (!wait_or_abort(br.v_full + s, (itk / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (k == 0 && !wait_or_abort(br.o_free + w, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (!wait_or_abort(br.p_full + w, pc & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      for (int w = 0; w < un.nact; ++w) {
-        if (k == 0 && !wait_or_abort(br.o_free + w, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
-        if (!wait_or_abort(br.p_full + w, pc[w] & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
-        const int pbuf = int(pc[w] & 1u);
-        ++pc[w];
-        tc_fence_after();
-        issue_PV(w, s, pbuf, k > 0);
+      const int pbuf = int(pc & 1u);
+#pragma unroll
+      for (int kk = 0; kk < T / 32; ++kk) {
+        const uint64_t da = smem_desc(aP + uint32_t((2 * w + pbuf) * C::PB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
+        const uint64_t db = smem_desc(aV + uint32_t(s * C::VB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
+        mma_f8_ss(tO, da, db, idO, (k > 0 || kk > 0) ? 1u : 0u);
       }
-      if (!ok) break;
+      mma_commit(br.o_done + 2 * w + (pc & 1u));
+      ++pc;
       mma_commit(br.v_empty + s);
     }
     it += uint32_t(un.nt);
@@ -317,8 +330,8 @@ __device__ __forceinline__ void mma_issuer(const Params& p, uint32_t tmem, uint8
     raise_abort(p, abort_flag);
     if (issued_any) {
       volatile int no_abort = 0;
-      mma_commit(br.drain);
-      wait_or_abort(br.drain, 0, kDrainNs, &no_abort);
+      mma_commit(br.drain + w);
+      wait_or_abort(br.drain + w, 0, kDrainNs, &no_abort);
     }
   }
 }
@@ -345,7 +358,11 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
   const uint32_t tS = tmem + lane_off + uint32_t(w * T);
   const uint32_t tO = tmem + lane_off + uint32_t(2 * T + w * D);
   uint8_t* my_p = sP + size_t(2 * w) * kRows * T;
-  uint32_t sc = 0, oc = 0, np = 0;  // S tiles read, P.V products waited for, P tiles written
+  uint32_t sc = 0, np = 0;  // S tiles read, P tiles written (= P.V products requested)
+  // wait for P.V product n of this warpgroup (barrier n % 2, its (n / 2)-th phase)
+  auto wait_pv = [&](uint32_t n) -> bool {
+    return warp_wait(br.o_done + 2 * w + (n & 1u), (n >> 1) & 1u, p, abort_flag);
+  };
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = decode_unit<T>(p, u);
@@ -402,8 +419,8 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       const float off = __fsub_rn(p.log2S, muse);
       const uint64_t off2 = pack2(off, off);
       uint64_t ls2[2] = {pack2(0.0f, 0.0f), pack2(0.0f, 0.0f)};
-      // codes go straight to P buffer np % 2 (its last reader, P.V of the tile
-      // before the previous one, completed before the previous tile's rescale)
+      // codes go straight to P buffer np % 2, whose last reader was product np - 2
+      if (np >= 2 && !wait_pv(np - 2)) { ok = false; break; }
       uint8_t* pbuf = my_p + size_t(np & 1u) * kRows * T;
 #pragma unroll
       for (int cch = 0; cch < T / 16; ++cch) {
@@ -440,36 +457,34 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       unpack2(ls2[0], la, lb);
       unpack2(ls2[1], lc, ld);
       l = __fadd_rn(__fmul_rn(alpha, l), __fadd_rn(__fadd_rn(la, lb), __fadd_rn(lc, ld)));
-      if (k > 0) {
-        // O_w += P_w(k-1) V(k-1) must be complete before O_w is rescaled.
-        if (!warp_wait(br.o_done + w, oc & 1u, p, abort_flag)) { ok = false; break; }
-        ++oc;
+      if (k > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        // O_w += P_w(k-1) V(k-1) (product np - 2 now) must be complete before
+        // O_w is rescaled; rows with alpha == 1 are multiplied by 1 (exact).
+        if (!wait_pv(np - 2)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-          const uint64_t a2 = pack2(alpha, alpha);
+        const uint64_t a2 = pack2(alpha, alpha);
 #pragma unroll 1
-          for (int q = 0; q < D / 64; ++q) {
-            uint32_t o0[32], o1[32];
-            tmem_ld32(tO + uint32_t(64 * q), o0);
-            tmem_ld32(tO + uint32_t(64 * q + 32), o1);
-            tmem_wait_ld();
-            reg_fence32(o0);
-            reg_fence32(o1);
+        for (int q = 0; q < D / 64; ++q) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tO + uint32_t(64 * q), o0);
+          tmem_ld32(tO + uint32_t(64 * q + 32), o1);
+          tmem_wait_ld();
+          reg_fence32(o0);
+          reg_fence32(o1);
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float x0, x1;
-              unpack2(fmul2(pack2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2), x0, x1);
-              o0[e] = __float_as_uint(x0);
-              o0[e + 1] = __float_as_uint(x1);
-              unpack2(fmul2(pack2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2), x0, x1);
-              o1[e] = __float_as_uint(x0);
-              o1[e + 1] = __float_as_uint(x1);
-            }
-            tmem_st32(tO + uint32_t(64 * q), o0);
-            tmem_st32(tO + uint32_t(64 * q + 32), o1);
+          for (int e = 0; e < 32; e += 2) {
+            float x0, x1;
+            unpack2(fmul2(pack2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2), x0, x1);
+            o0[e] = __float_as_uint(x0);
+            o0[e + 1] = __float_as_uint(x1);
+            unpack2(fmul2(pack2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2), x0, x1);
+            o1[e] = __float_as_uint(x0);
+            o1[e + 1] = __float_as_uint(x1);
           }
-          tmem_wait_st();
+          tmem_st32(tO + uint32_t(64 * q), o0);
+          tmem_st32(tO + uint32_t(64 * q + 32), o1);
         }
+        tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -478,8 +493,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
     }
     if (!ok) break;
     // epilogue: O = acc * dv / (S * l); the running sum already holds S * l
-    if (!warp_wait(br.o_done + w, oc & 1u, p, abort_flag)) { ok = false; break; }
-    ++oc;
+    if (!wait_pv(np - 1)) { ok = false; break; }
     tc_fence_after();
     const float scale = __fdiv_rn(p.v_ds[bg], l);
 #pragma unroll 1
@@ -553,31 +567,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   br.s_free = br.s_full + 2;
   br.p_full = br.s_free + 2;
   br.o_done = br.p_full + 2;
-  br.o_free = br.o_done + 2;
+  br.o_free = br.o_done + 4;
   br.drain = br.o_free + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(br.drain + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(br.drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(br.q_full + b, 1);
-      mbar_init(br.q_empty + b, 1);
+      mbar_init(br.q_empty + b, 2);
     }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(br.k_full + s, 1);
-      mbar_init(br.k_empty + s, 1);
+      mbar_init(br.k_empty + s, 2);
       mbar_init(br.v_full + s, 1);
-      mbar_init(br.v_empty + s, 1);
+      mbar_init(br.v_empty + s, 2);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(br.s_full + w, 1);
       mbar_init(br.s_free + w, 128);
       mbar_init(br.p_full + w, 128);
-      mbar_init(br.o_done + w, 1);
+      mbar_init(br.o_done + 2 * w, 1);
+      mbar_init(br.o_done + 2 * w + 1, 1);
       mbar_init(br.o_free + w, 128);
+      mbar_init(br.drain + w, 1);
     }
-    mbar_init(br.drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -599,8 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kControlRegs>();
     if (warp == kProducerWarp) {
       if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
-    } else if (warp == kMmaWarp) {
-      if (lane == 0) mma_issuer<D, T>(p, tmem, sQ, sP, sK, sV, br, abort_flag);
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+      if (lane == 0) mma_issuer<D, T>(p, warp - kMmaWarp, tmem, sQ, sP, sK, sV, br, abort_flag);
     }
   } else {
     regs_increase<kSoftmaxRegs>();
