@@ -431,8 +431,12 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
           float PS[4];
           unpack2(ffma2(pack2(sv[4 * q], sv[4 * q + 1]), c2, off2), PS[0], PS[1]);
           unpack2(ffma2(pack2(sv[4 * q + 2], sv[4 * q + 3]), c2, off2), PS[2], PS[3]);
+          // Without counters the flush-to-zero form is exact for the output: a
+          // P*S below 2^-126 casts to the E4M3 code 0 either way, and its share
+          // of the row sum is below fp32 resolution.  The counting build keeps
+          // subnormal P*S, whose cast to 0 it must count.
 #pragma unroll
-          for (int e = 0; e < 4; ++e) PS[e] = ex2(PS[e]);
+          for (int e = 0; e < 4; ++e) PS[e] = COUNT ? ex2(PS[e]) : ex2_ftz(PS[e]);
           ls2[0] = fadd2(ls2[0], pack2(PS[0], PS[1]));
           ls2[1] = fadd2(ls2[1], pack2(PS[2], PS[3]));
           pw[qq] = pack_b16x2(cvt_e4m3x2(PS[0], PS[1]), cvt_e4m3x2(PS[2], PS[3]));

@@ -321,4 +321,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x, hardware approximation, results below 2^-126 flushed to zero: a single
+// MUFU operation (the form above adds a subnormal fix-up around it).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace attnq
