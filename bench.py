@@ -87,6 +87,15 @@ def ncu_traffic(kernel: str, src_hash: str):
     return None
 
 
+def launches_per_step(flags: int) -> int:
+    """Kernels one prepare + forward step launches: mean key (partial sums and
+    final, or a zero fill without centring), amax, scales, cast, the
+    transposed V cast with ATTNQ_VT_LAYOUT, and the attention kernel."""
+    import precision_attention_numerics_gb300 as aq
+    n = (2 if flags & aq.ATTNQ_CENTER_K else 1) + 3 + 1
+    return n + (1 if flags & aq.ATTNQ_VT_LAYOUT else 0)
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling while the timed region runs."""
 
@@ -348,7 +357,7 @@ def run_ours(args):
         # per-head error against FP64 on a row sample (oracle, outside the timed region)
         import oracle
         rows = np.unique(np.array([0, 1, 127, 4095, N // 2 - 1, N // 2, N - 1], dtype=np.int64))
-        bh = sorted({0, B * Hq // 2 - 1, B * Hq // 2 + 5, B * Hq - 1})
+        bh = sorted({h for h in (0, B * Hq // 2 - 1, B * Hq // 2 + 5, B * Hq - 1) if 0 <= h < B * Hq})
         Og = O.view(B * Hq, N, d)[bh][:, rows].float().cpu().numpy().astype(np.float64)
         exact = oracle.attn_exact(q_np, k_np, v_np, bh_list=bh, rows=rows)
         rel = np.linalg.norm(Og - exact, axis=(1, 2)) / np.linalg.norm(exact, axis=(1, 2))
@@ -387,7 +396,7 @@ def run_ours(args):
                 "value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_elapsed / args.steps * 1e3},
             "clocks": clocks,
-            "gpu_launches": args.steps * (7 if flags & aq.ATTNQ_CENTER_K else 5),
+            "gpu_launches": args.steps * launches_per_step(flags),
         }
     if dist is not None:
         dist.barrier()

@@ -45,7 +45,9 @@
 //                                                          -> MMA issues O_w += P_w(k) V(k)
 // P.V completions alternate between two barriers per warpgroup (product n
 // on barrier n % 2), so the softmax waits only for the products it needs:
-// product n-2 before reusing its P buffer, n-1 before a rescale.
+// product n-2 before reusing its P buffer, n-1 before a rescale.  "P ready"
+// alternates the same way, because a warpgroup's warps drift apart by up to
+// one tile.
 // so S_w(k+1) and the P.V products run on the tensor core while the softmax
 // warps compute, and the softmax never waits for its own S(k+1) MMA.
 //
@@ -104,7 +106,7 @@ struct Cfg {
   static constexpr uint32_t SBO_QK = 8u * D;
   static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;    // V^T and P rows are T bytes
   static constexpr uint32_t SBO_V = 8u * T;
-  static constexpr int NBARS = 4 + 4 * NS + 12 + 2;
+  static constexpr int NBARS = 4 + 4 * NS + 14 + 2;
   static constexpr size_t SMEM = 1024 + 4 * size_t(QB) + 4 * size_t(PB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -141,7 +143,7 @@ struct Bars {
   uint64_t* v_empty;
   uint64_t* s_full;  // [2] S_w in TMEM (MMA commit)
   uint64_t* s_free;  // [2] S_w read by its warpgroup (128 arrivals)
-  uint64_t* p_full;  // [2] P_w in shared memory and O_w rescaled (128 arrivals)
+  uint64_t* p_full;  // [2][2] P_w tile n written and O_w rescaled, on [w][n % 2] (128 arrivals)
   uint64_t* o_done;  // [2][2] O_w += P_w V of product n complete, on [w][n % 2] (MMA commit)
   uint64_t* o_free;  // [2] O_w read by the epilogue (128 arrivals)
   uint64_t* drain;
@@ -168,9 +170,12 @@ __device__ __forceinline__ void raise_abort(const Params& p, volatile int* abort
   }
 }
 
-// Warp-uniform wait: lane 0 polls, the verdict is broadcast.
+// Warp-uniform wait.  Fast path: every lane tests the barrier and the warp
+// votes (no divergence, no broadcast); otherwise lane 0 waits with the bound
+// and the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
                                           volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   uint32_t ok = 0;
   if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, p.wait_ns, abort_flag) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -250,6 +255,7 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
   int uc = 0;
   uint32_t n_s = 0;  // S MMAs issued (whole kernel)
   uint32_t pc = 0;   // P.V products issued (whole kernel)
+  uint32_t act = 0;  // units this warpgroup took part in (one o_free phase each)
   bool ok = true;
   bool issued_any = false;
 
@@ -310,8 +316,10 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
       }
       const int s = int(itk % C::NS);
       if (!wait_or_abort(br.v_full + s, (itk / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
-      if (k == 0 && !wait_or_abort(br.o_free + w, (uc & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
-      if (!wait_or_abort(br.p_full + w, pc & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      // O_w is overwritten by the unit's first product: the epilogue of the
+      // warpgroup's previous unit must have read it
+      if (k == 0 && !wait_or_abort(br.o_free + w, (act & 1u) ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (!wait_or_abort(br.p_full + 2 * w + (pc & 1u), (pc >> 1) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const int pbuf = int(pc & 1u);
 #pragma unroll
@@ -325,6 +333,7 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
       mma_commit(br.v_empty + s);
     }
     it += uint32_t(un.nt);
+    ++act;
   }
   if (!ok) {
     raise_abort(p, abort_flag);
@@ -366,10 +375,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
   bool ok = true;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
     const Unit un = decode_unit<T>(p, u);
-    if (w >= un.nact) {
-      mbar_arrive(br.o_free + w);
-      continue;
-    }
+    if (w >= un.nact) continue;  // sits the unit out: no arrival on o_free (its warps would not be in step)
     const int h = un.h0 + w;
     const int bh = un.b * p.Hq + h, bg = un.b * p.Hkv + un.g;
     const float c = __double2float_rn(
@@ -490,9 +496,12 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
         }
         tmem_wait_st();
       }
+      // The warps of a warpgroup are not in step: a warp may write P(n+1) and
+      // arrive while another is still on P(n).  Alternating barriers keep
+      // those arrivals apart (none can reach P(n+2) before P.V(n) is done).
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(br.p_full + w);
+      mbar_arrive(br.p_full + 2 * w + ((np - 1) & 1u));
       m = mnew;
     }
     if (!ok) break;
@@ -570,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   br.s_full = br.v_empty + C::NS;
   br.s_free = br.s_full + 2;
   br.p_full = br.s_free + 2;
-  br.o_done = br.p_full + 2;
+  br.o_done = br.p_full + 4;
   br.o_free = br.o_done + 4;
   br.drain = br.o_free + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(br.drain + 2);
@@ -591,7 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < 2; ++w) {
       mbar_init(br.s_full + w, 1);
       mbar_init(br.s_free + w, 128);
-      mbar_init(br.p_full + w, 128);
+      mbar_init(br.p_full + 2 * w, 128);
+      mbar_init(br.p_full + 2 * w + 1, 128);
       mbar_init(br.o_done + 2 * w, 1);
       mbar_init(br.o_done + 2 * w + 1, 1);
       mbar_init(br.o_free + w, 128);

@@ -111,3 +111,19 @@ def test_rejects_bad_arguments():
             aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, args["S"], args["kv_order"], args["causal"],
                          args["kv_tile"], O)
         assert e.value.code == code
+
+
+@pytest.mark.parametrize("Hq,Hkv,d", [(4, 1, 64), (8, 2, 128), (7, 1, 128)])
+def test_repeated_calls_are_bitwise_identical(Hq, Hkv, d):
+    """Each row is owned by one thread and every reduction has a fixed order,
+    so repeated launches must agree bit for bit; a race between warps of a
+    warpgroup (a stale P tile, an unsynchronised rescale) shows up here."""
+    from tests.gpu_helpers import gpu_fwd, gpu_prepare
+    q, k, v = synth.qwen_like_inputs(120 + Hq, 2, Hq, Hkv, 1000, d, key_norm=30.0, key_channels=4)
+    desc, bufs, _ = gpu_prepare(q, k, v, 3, synth.hadamard_signs(5, d))
+    first, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, 128, count=False)
+    assert st == 0
+    for _ in range(8):
+        again, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, 128, count=False)
+        assert st == 0
+        assert torch.equal(first, again)
