@@ -26,9 +26,11 @@
 //   warp 8     TMA producer: Q tiles once per unit (two buffers, so the next
 //              unit's Q loads during this one), K and V^T tiles through an
 //              NS-stage ring
-//   warp 9     TMEM allocator; lane 0 issues warpgroup 0's MMAs
-//   warp 10    lane 0 issues warpgroup 1's MMAs (each warpgroup's MMAs are
-//              in order; the two streams do not wait for each other)
+//   warp 9     TMEM allocator; issues warpgroup 0's MMAs
+//   warp 10    issues warpgroup 1's MMAs (each warpgroup's MMAs are in
+//              order; the two streams do not wait for each other).  The MMA
+//              warps run converged and let one elected lane issue: a lone
+//              lane takes about twice as long per MMA.
 // TMEM columns: S_w at [w*T, w*T+T), O_w at [2T + w*D, 2T + w*D + D).
 // Shared memory: Q[2 buffers][2 warpgroups], P[2 warpgroups][2 buffers] (the
 // E4M3 probabilities, written by the softmax threads in the 128-byte (or
@@ -68,9 +70,9 @@ constexpr int kRows = 128;
 constexpr int kThreads = 384;          // three warpgroups
 constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of warpgroups 0 and 1
 // Register split: launched at 168 per thread (384 x 168 = 64,512); the two
-// softmax warpgroups rise to 224, warpgroup 2 (producer, MMA, two idle warps)
-// drops to 56: 2 x 128 x 224 + 128 x 56 = 64,512.
-constexpr uint32_t kSoftmaxRegs = 224, kControlRegs = 56;
+// softmax warpgroups rise to 208, warpgroup 2 (producer, the two MMA warps,
+// one idle warp) drops to 88: 2 x 128 x 208 + 128 x 88 = 64,512.
+constexpr uint32_t kSoftmaxRegs = 208, kControlRegs = 88;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
 // Bound for draining in-flight copies and MMAs after an abort (independent of
 // the wait limit, so an abort never leaves copies in flight).
@@ -240,37 +242,68 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
   }
 }
 
-// Issues the MMAs of warpgroup w.  K/V stage and Q buffer barriers take one
-// arrival from each of the two issuing threads (a commit when the thread's
-// warpgroup used them, a plain arrive when it sat the unit out).
+// Wait for a converged warp: every lane waits (they sleep in try_wait) and
+// the verdict is voted, so the warp leaves converged.
+__device__ __forceinline__ bool vote_wait(uint64_t* bar, uint32_t parity, const Params& p, volatile int* abort_flag) {
+  const bool ok = wait_or_abort(bar, parity, p.wait_ns, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Position in the K/V stage ring: stage s, and the parity of its current use.
+struct Ring {
+  uint32_t s, ph;
+  __device__ __forceinline__ void next(uint32_t ns) {
+    if (++s == ns) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// Issues the MMAs of warpgroup w.  Run by a whole, converged warp: waits are
+// voted, the elected lane issues each MMA and commit, and the shared
+// memory descriptors are built from a low word stepped by (byte offset >> 4)
+// in its start address field (every address stays below 256 KB, so the field
+// never carries) and a constant high word.
+// K/V stage and Q buffer barriers take one arrival from each of the two
+// issuing warps (a commit when the warp's warpgroup used them, a plain arrive
+// when it sat the unit out).
 template <int D, int T>
 __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem, uint8_t* sQ, uint8_t* sP,
                                            uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
   using C = Cfg<D, T>;
   constexpr uint32_t idS = idesc_e4m3_f32(kRows, T);
   constexpr uint32_t idO = idesc_e4m3_f32(kRows, D);
-  const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aK = smem_u32(sK), aV = smem_u32(sV);
+  // descriptor = {start address field (low word), constant high word}
+  const uint32_t hQK = uint32_t(smem_desc(0, 16, C::SBO_QK, C::LAYOUT_QK) >> 32);
+  const uint32_t hV = uint32_t(smem_desc(0, 16, C::SBO_V, C::LAYOUT_V) >> 32);
+  const uint32_t lQ0 = uint32_t(smem_desc(smem_u32(sQ) + uint32_t(w * C::QB), 16, C::SBO_QK, C::LAYOUT_QK));
+  const uint32_t lK0 = uint32_t(smem_desc(smem_u32(sK), 16, C::SBO_QK, C::LAYOUT_QK));
+  const uint32_t lP0 = uint32_t(smem_desc(smem_u32(sP) + uint32_t(2 * w * C::PB), 16, C::SBO_V, C::LAYOUT_V));
+  const uint32_t lV0 = uint32_t(smem_desc(smem_u32(sV), 16, C::SBO_V, C::LAYOUT_V));
   const uint32_t tS = tmem + uint32_t(w * T), tO = tmem + uint32_t(2 * T + w * D);
-  uint32_t it = 0;
+  Ring rk{0u, 0u}, rv{0u, 0u};  // next K stage for an S product, next V stage for a P.V product
   int uc = 0;
-  uint32_t n_s = 0;  // S MMAs issued (whole kernel)
+  uint32_t n_s = 0;  // S products issued (whole kernel)
   uint32_t pc = 0;   // P.V products issued (whole kernel)
   uint32_t act = 0;  // units this warpgroup took part in (one o_free phase each)
   bool ok = true;
   bool issued_any = false;
 
-  // S_w = Q_w K^T; the previous S_w must have been read by the warpgroup.
-  auto issue_S = [&](int s, int qb) -> bool {
-    if (n_s > 0 && !wait_or_abort(br.s_free + w, (n_s - 1) & 1u, p.wait_ns, abort_flag)) return false;
+  // S_w = Q_w K^T from K stage rk.s; the previous S_w must have been read by
+  // the warpgroup.  Releases the K stage when the product completes.
+  auto issue_S = [&](uint32_t lq) -> bool {
+    if (!vote_wait(br.k_full + rk.s, rk.ph, p, abort_flag)) return false;
+    if (n_s > 0 && !vote_wait(br.s_free + w, (n_s - 1) & 1u, p, abort_flag)) return false;
     ++n_s;
     tc_fence_after();
+    const uint32_t lk = lK0 + rk.s * uint32_t(C::KB >> 4);
 #pragma unroll
-    for (int kk = 0; kk < D / 32; ++kk) {
-      const uint64_t da = smem_desc(aQ + uint32_t((2 * qb + w) * C::QB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
-      const uint64_t db = smem_desc(aK + uint32_t(s * C::KB + 32 * kk), 16, C::SBO_QK, C::LAYOUT_QK);
-      mma_f8_ss(tS, da, db, idS, kk > 0 ? 1u : 0u);
-    }
-    mma_commit(br.s_full + w);
+    for (int kk = 0; kk < D / 32; ++kk)
+      mma_f8_ss_elect(tS, pack_desc(lq + 2 * kk, hQK), pack_desc(lk + 2 * kk, hQK), idS, kk > 0 ? 1u : 0u);
+    mma_commit_elect(br.s_full + w);
+    mma_commit_elect(br.k_empty + rk.s);
+    rk.next(C::NS);
     issued_any = true;
     return true;
   };
@@ -278,69 +311,54 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
     const Unit un = decode_unit<T>(p, u);
     const int qb = uc & 1;
-    if (!wait_or_abort(br.q_full + qb, (uc >> 1) & 1, p.wait_ns, abort_flag)) { ok = false; break; }
+    if (!vote_wait(br.q_full + qb, (uc >> 1) & 1, p, abort_flag)) { ok = false; break; }
     tc_fence_after();
     if (w >= un.nact) {
       // this warpgroup sits the unit out: release each stage and the Q buffer
       for (int k = 0; k < un.nt && ok; ++k) {
-        const uint32_t itk = it + uint32_t(k);
-        const int s = int(itk % C::NS);
-        const uint32_t ph = (itk / C::NS) & 1u;
-        if (!wait_or_abort(br.k_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
-        mbar_arrive(br.k_empty + s);
-        if (!wait_or_abort(br.v_full + s, ph, p.wait_ns, abort_flag)) { ok = false; break; }
-        mbar_arrive(br.v_empty + s);
+        if (!vote_wait(br.k_full + rk.s, rk.ph, p, abort_flag)) { ok = false; break; }
+        mbar_arrive_elect(br.k_empty + rk.s);
+        rk.next(C::NS);
+        if (!vote_wait(br.v_full + rv.s, rv.ph, p, abort_flag)) { ok = false; break; }
+        mbar_arrive_elect(br.v_empty + rv.s);
+        rv.next(C::NS);
       }
-      mbar_arrive(br.q_empty + qb);
-      it += uint32_t(un.nt);
+      mbar_arrive_elect(br.q_empty + qb);
       continue;
     }
-    {
-      const int s = int(it % C::NS);
-      if (!wait_or_abort(br.k_full + s, (it / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      if (!issue_S(s, qb)) { ok = false; break; }
-      mma_commit(br.k_empty + s);
-      if (un.nt == 1) mma_commit(br.q_empty + qb);
-    }
+    const uint32_t lq = lQ0 + uint32_t(qb * (2 * C::QB >> 4));
+    if (!issue_S(lq)) { ok = false; break; }
+    if (un.nt == 1) mma_commit_elect(br.q_empty + qb);
     for (int k = 0; k < un.nt && ok; ++k) {
-      const uint32_t itk = it + uint32_t(k);
       if (k + 1 < un.nt) {
-        const uint32_t it1 = itk + 1;
-        const int s1 = int(it1 % C::NS);
-        if (!wait_or_abort(br.k_full + s1, (it1 / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        if (!issue_S(s1, qb)) { ok = false; break; }
-        mma_commit(br.k_empty + s1);
-        if (k + 1 == un.nt - 1) mma_commit(br.q_empty + qb);
+        if (!issue_S(lq)) { ok = false; break; }
+        if (k + 1 == un.nt - 1) mma_commit_elect(br.q_empty + qb);
       }
-      const int s = int(itk % C::NS);
-      if (!wait_or_abort(br.v_full + s, (itk / C::NS) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (!vote_wait(br.v_full + rv.s, rv.ph, p, abort_flag)) { ok = false; break; }
       // O_w is overwritten by the unit's first product: the epilogue of the
       // warpgroup's previous unit must have read it
-      if (k == 0 && !wait_or_abort(br.o_free + w, (act & 1u) ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
-      if (!wait_or_abort(br.p_full + 2 * w + (pc & 1u), (pc >> 1) & 1u, p.wait_ns, abort_flag)) { ok = false; break; }
+      if (k == 0 && !vote_wait(br.o_free + w, (act & 1u) ^ 1u, p, abort_flag)) { ok = false; break; }
+      if (!vote_wait(br.p_full + 2 * w + (pc & 1u), (pc >> 1) & 1u, p, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const int pbuf = int(pc & 1u);
+      const uint32_t lp = lP0 + (pc & 1u) * uint32_t(C::PB >> 4);
+      const uint32_t lv = lV0 + rv.s * uint32_t(C::VB >> 4);
 #pragma unroll
-      for (int kk = 0; kk < T / 32; ++kk) {
-        const uint64_t da = smem_desc(aP + uint32_t((2 * w + pbuf) * C::PB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
-        const uint64_t db = smem_desc(aV + uint32_t(s * C::VB + 32 * kk), 16, C::SBO_V, C::LAYOUT_V);
-        mma_f8_ss(tO, da, db, idO, (k > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(br.o_done + 2 * w + (pc & 1u));
+      for (int kk = 0; kk < T / 32; ++kk)
+        mma_f8_ss_elect(tO, pack_desc(lp + 2 * kk, hV), pack_desc(lv + 2 * kk, hV), idO, (k > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(br.o_done + 2 * w + (pc & 1u));
       ++pc;
-      mma_commit(br.v_empty + s);
+      mma_commit_elect(br.v_empty + rv.s);
+      rv.next(C::NS);
     }
-    it += uint32_t(un.nt);
     ++act;
   }
   if (!ok) {
-    raise_abort(p, abort_flag);
+    if ((threadIdx.x & 31) == 0) raise_abort(p, abort_flag);
     if (issued_any) {
       volatile int no_abort = 0;
-      mma_commit(br.drain + w);
-      wait_or_abort(br.drain + w, 0, kDrainNs, &no_abort);
+      mma_commit_elect(br.drain + w);
+      if ((threadIdx.x & 31) == 0) wait_or_abort(br.drain + w, 0, kDrainNs, &no_abort);
+      __syncwarp();
     }
   }
 }
@@ -629,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
       if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      if (lane == 0) mma_issuer<D, T>(p, warp - kMmaWarp, tmem, sQ, sP, sK, sV, br, abort_flag);
+      mma_issuer<D, T>(p, warp - kMmaWarp, tmem, sQ, sP, sK, sV, br, abort_flag);
     }
   } else {
     regs_increase<kSoftmaxRegs>();
