@@ -426,15 +426,17 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
         for (int j = 0; j < T; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
       }
       // row max of the raw sums: fl32(s * c) is monotone in s for c > 0
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // eight independent two-input chains (the three-input form measured slower)
+      float mx[8];
 #pragma unroll
-      for (int j = 0; j < T; j += 8) {
-        mx[0] = fmax3(mx[0], sv[j], sv[j + 1]);
-        mx[1] = fmax3(mx[1], sv[j + 2], sv[j + 3]);
-        mx[2] = fmax3(mx[2], sv[j + 4], sv[j + 5]);
-        mx[3] = fmax3(mx[3], sv[j + 6], sv[j + 7]);
+      for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+#pragma unroll
+      for (int j = 8; j < T; j += 8) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
       }
-      const float smax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mt = (smax == -INFINITY) ? -INFINITY : __fmul_rn(smax, c);
       const float mnew = fmaxf(m, mt);
       const float muse = (mnew == -INFINITY) ? 0.0f : mnew;
@@ -491,27 +493,22 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
         if (!wait_pv(np - 2)) { ok = false; break; }
         tc_fence_after();
         const uint64_t a2 = pack2(alpha, alpha);
-#pragma unroll 1
-        for (int q = 0; q < D / 64; ++q) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tO + uint32_t(64 * q), o0);
-          tmem_ld32(tO + uint32_t(64 * q + 32), o1);
-          tmem_wait_ld();
-          reg_fence32(o0);
-          reg_fence32(o1);
+        // all D columns of the row in one round trip (the scores are dead here)
+        uint32_t o[D];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float x0, x1;
-            unpack2(fmul2(pack2(__uint_as_float(o0[e]), __uint_as_float(o0[e + 1])), a2), x0, x1);
-            o0[e] = __float_as_uint(x0);
-            o0[e + 1] = __float_as_uint(x1);
-            unpack2(fmul2(pack2(__uint_as_float(o1[e]), __uint_as_float(o1[e + 1])), a2), x0, x1);
-            o1[e] = __float_as_uint(x0);
-            o1[e + 1] = __float_as_uint(x1);
-          }
-          tmem_st32(tO + uint32_t(64 * q), o0);
-          tmem_st32(tO + uint32_t(64 * q + 32), o1);
+        for (int q = 0; q < D / 32; ++q) tmem_ld32(tO + uint32_t(32 * q), *reinterpret_cast<uint32_t(*)[32]>(&o[32 * q]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&o[32 * q]));
+#pragma unroll
+        for (int e = 0; e < D; e += 2) {
+          float x0, x1;
+          unpack2(fmul2(pack2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), x0, x1);
+          o[e] = __float_as_uint(x0);
+          o[e + 1] = __float_as_uint(x1);
         }
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) tmem_st32(tO + uint32_t(32 * q), *reinterpret_cast<uint32_t(*)[32]>(&o[32 * q]));
         tmem_wait_st();
       }
       // The warps of a warpgroup are not in step: a warp may write P(n+1) and
