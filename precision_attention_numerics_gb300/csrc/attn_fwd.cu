@@ -409,29 +409,46 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       if (!warp_wait(br.s_full + w, sc & 1u, p, abort_flag)) { ok = false; break; }
       ++sc;
       tc_fence_after();
+      const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
+      // keys j0 + j are visible for j < lim (causal: j0 + j <= i; always j0 + j < N)
+      const int lim = need_mask ? min(p.N - j0, p.causal ? i - j0 + 1 : T) : T;
+      // S in two halves: the row max of the first half runs while the second
+      // half is still on its way out of TMEM
+      constexpr int H = T / 2;
       float sv[T];
 #pragma unroll
-      for (int q = 0; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      for (int q = 0; q < H / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
       tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
-      // S_w is in registers: the MMA thread may overwrite it with the next tile
-      tc_fence_before();
-      mbar_arrive(br.s_free + w);
-      const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
-      if (need_mask) {
-        // keys j0 + j are visible for j < lim (causal: j0 + j <= i; always j0 + j < N)
-        const int lim = min(p.N - j0, p.causal ? i - j0 + 1 : T);
+      for (int q = 0; q < H / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
 #pragma unroll
-        for (int j = 0; j < T; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
+      for (int q = H / 32; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      if (need_mask) {
+#pragma unroll
+        for (int j = 0; j < H; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
       }
-      // row max of the raw sums: fl32(s * c) is monotone in s for c > 0
+      // row max of the raw sums (fl32(s * c) is monotone in s for c > 0):
       // eight independent two-input chains (the three-input form measured slower)
       float mx[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = sv[e];
 #pragma unroll
-      for (int j = 8; j < T; j += 8) {
+      for (int j = 8; j < H; j += 8) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int q = H / 32; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+      // S_w is in registers: the MMA warp may overwrite it with the next tile
+      tc_fence_before();
+      mbar_arrive(br.s_free + w);
+      if (need_mask) {
+#pragma unroll
+        for (int j = H; j < T; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
+      }
+#pragma unroll
+      for (int j = H; j < T; j += 8) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
       }
@@ -445,8 +462,10 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       const float off = __fsub_rn(p.log2S, muse);
       const uint64_t off2 = pack2(off, off);
       uint64_t ls2[2] = {pack2(0.0f, 0.0f), pack2(0.0f, 0.0f)};
-      // codes go straight to P buffer np % 2, whose last reader was product np - 2
-      if (np >= 2 && !wait_pv(np - 2)) { ok = false; break; }
+      // Codes go straight to P buffer np % 2, whose last reader was product
+      // np - 2.  No wait is needed: the MMA warp issued P.V np - 2 before
+      // S np, and the commit that signalled "S np complete" covers every
+      // earlier tcgen05 operation of that warp.
       uint8_t* pbuf = my_p + size_t(np & 1u) * kRows * T;
 #pragma unroll
       for (int cch = 0; cch < T / 16; ++cch) {
