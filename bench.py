@@ -88,12 +88,10 @@ def ncu_traffic(kernel: str, src_hash: str):
 
 
 def launches_per_step(flags: int) -> int:
-    """Kernels one prepare + forward step launches: mean key (partial sums and
-    final, or a zero fill without centring), amax, scales, cast, the
-    transposed V cast with ATTNQ_VT_LAYOUT, and the attention kernel."""
-    import precision_attention_numerics_gb300 as aq
-    n = (2 if flags & aq.ATTNQ_CENTER_K else 1) + 3 + 1
-    return n + (1 if flags & aq.ATTNQ_VT_LAYOUT else 0)
+    """Kernels one prepare + forward step launches: the prepare's
+    initialisation (counters and work list) and its persistent kernel, then
+    the attention kernel."""
+    return 3
 
 
 class ClockSampler:

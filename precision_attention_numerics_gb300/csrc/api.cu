@@ -171,6 +171,8 @@ attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K,
   a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
   a.ldv = attnq_vt_ld(desc->N);
   a.status = g_status_ptr[dev];
+  a.num_sms = g_num_sms[dev];
+  a.wait_ns = g_wait_ns;
   carve_prepare_workspace(a, workspace);
   return from_cuda(launch_prepare(a, stream));
 }
@@ -204,7 +206,9 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
   a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
   a.ldv = attnq_vt_ld(desc->N);
   a.status = g_status_ptr[dev];
-  carve_prepare_workspace(a, scratch);   // the amax words are cleared by the launch itself
+  a.num_sms = g_num_sms[dev];
+  a.wait_ns = g_wait_ns;
+  carve_prepare_workspace(a, scratch);   // the launch itself clears the counters it uses
   return from_cuda(launch_prepare(a, stream));
 }
 

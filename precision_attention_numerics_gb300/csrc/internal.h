@@ -28,9 +28,17 @@ struct PrepareArgs {
   // workspace carve-up
   uint32_t* amax_bits;  // [nslices]
   float* qs;            // [nslices]
+  uint32_t* a_done;     // [nslices] tiles whose amax is in amax_bits
+  uint32_t* s_ready;    // [nslices] scale published
+  uint32_t* m_done;     // [B*Hkv] mean-key chunks summed
+  uint32_t* mu_ready;   // [B*Hkv] mean key published
+  uint32_t* ctl;        // [4] ticket, abort, number of entries
+  uint32_t* entries;    // [3*nslices] work list: kind << 30 | slice
   float* mean_part;     // [B*Hkv*nchunks*d]
   float* mu;            // [B*Hkv*d]
   uint32_t* status;
+  int num_sms;
+  uint64_t wait_ns;
 };
 
 size_t prepare_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int center);

@@ -1,15 +1,35 @@
-// Operand preparation kernels ("attention-numerics" project page, method and
-// kernel settings; "A rounding problem, not a rotation problem", 01 /
-// Synthetic illustration):
+// Operand preparation ("attention-numerics" project page, method and kernel
+// settings; "A rounding problem, not a rotation problem", 01 / Synthetic
+// illustration):
 //   mean key (K, optional) -> sign flip + unnormalised FWHT (Q, K, optional)
 //   -> per-(batch, head) amax -> qs = 448/amax -> E4M3 RNE-satfinite cast.
 //
-// Bit-exactness: every float operation here is a single IEEE add, subtract,
-// multiply or divide in a fixed order (no contraction is possible: no
-// multiply feeds an add), the FWHT uses a fixed butterfly schedule, the max
-// is order-free, and the mean follows the fixed chunk order.  The HBM passes
-// read the inputs with 16-byte loads and write 8-byte E4M3 groups; a warp
-// covers two (d = 128) or four (d = 64) rows.
+// Bit-exactness: every float operation is a single IEEE add, subtract,
+// multiply or divide in a fixed order (subtractions are fma(b, -1, a), which
+// rounds a - b once), the FWHT uses the fixed butterfly schedule h = 1, 2, ...,
+// d/2, the max is order-free, and the mean follows the fixed chunk order
+// (128-token chunk sums in token order, then the chunk sums in order).
+//
+// One persistent kernel does every pass.  The work is a list of entries, one
+// per (pass, slice), where a slice is one (batch, head) of Q, K or V and the
+// passes are M (mean-key chunk sums, K with centring), A (amax) and C (cast).
+// An entry's slice is cut into items of four 128-row tiles; CTAs claim items
+// in list order with an atomic ticket.  The list puts each slice's A entry a
+// few steps after its M entry and its C entry a few steps after its A entry,
+// so a slice's second and third reads come from L2, and a pass waits only on
+// entries claimed before it (the finisher of a slice's last A tile publishes
+// its scale; the finisher of a K slice's last M tile publishes its mean): the
+// earliest unfinished item never waits, so the kernel cannot deadlock, and
+// it needs no co-residency.
+//
+// CTA: warp 8 claims items and streams their tiles into a ring of shared
+// memory stages with TMA (128-byte swizzle, rows beyond N read as zero);
+// warps 0-3 and 4-7 are two consumer groups that take alternate tiles, one
+// row per thread.  A row of d values is held as d/2 packed pairs
+// (x_j, x_{j+d/2}), so stages h = 1 .. d/4 of the FWHT are packed f32x2
+// adds and subtracts and stage d/2 adds the two halves of each pair.  Casts
+// go to shared memory in the 128- (or 64-) byte swizzled layout and leave by
+// TMA store; V in the transposed layout is written channel-major.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -20,169 +40,131 @@
 namespace attnq {
 namespace {
 
-constexpr int kMeanChunk = 128;   // tokens per partial sum of the mean key
-constexpr int kThreads = 256;
+constexpr int kTR = 128;           // rows per tile = tokens per mean-key chunk
+constexpr int kTilesPerItem = 4;   // tiles per claimed item
+constexpr int kGroups = 2;         // consumer groups (128 threads, one row each)
+constexpr int kFlowThreads = 32 * (4 * kGroups + 1);
+constexpr int kLagA = 4, kLagC = 3;  // list steps from a slice's M entry to its A entry, and A to C
+constexpr uint32_t KIND_M = 0u, KIND_A = 1u, KIND_C = 2u, KIND_DONE = 3u;
+constexpr uint32_t CTL_TICKET = 0, CTL_ABORT = 1, CTL_ENTRIES = 2;
 
-template <bool BF16>
-__device__ __forceinline__ void load8(const void* base, int64_t off, float (&x)[8]) {
-  if constexpr (BF16) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  } else {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
-    const float4 a = __ldg(p), b = __ldg(p + 1);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  }
-}
-
-template <bool BF16>
-__device__ __forceinline__ float load1(const void* base, int64_t off) {
-  if constexpr (BF16) {
-    return __uint_as_float(uint32_t(__ldg(static_cast<const uint16_t*>(base) + off)) << 16);
-  } else {
-    return __ldg(static_cast<const float*>(base) + off);
-  }
-}
-
-// x holds elements 8*sub .. 8*sub+7 of one row; the row's D/8 lanes are
-// consecutive and aligned in the warp.  All 32 lanes must call this.
-template <int D>
-__device__ __forceinline__ void transform(float (&x)[8], int sub, bool center, const float (&mu)[8], bool rotate,
-                                          const int8_t (&sg)[8]) {
-  if (center) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = __fsub_rn(x[e], mu[e]);
-  }
-  if (rotate) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = sg[e] < 0 ? -x[e] : x[e];
-    // butterfly stages h = 1, 2, 4 inside the lane
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 8; i += 2 * h) {
-#pragma unroll
-        for (int j = i; j < i + h; ++j) {
-          const float a = x[j], b = x[j + h];
-          x[j] = __fadd_rn(a, b);
-          x[j + h] = __fsub_rn(a, b);
-        }
-      }
-    }
-    // stages h = 8, 16, ..., D/2 across lanes: partner lane sub ^ (h/8)
-#pragma unroll
-    for (int m = 1; m < D / 8; m <<= 1) {
-      const bool upper = (sub & m) != 0;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
-        x[e] = upper ? __fsub_rn(o, x[e]) : __fadd_rn(x[e], o);
-      }
-    }
-  }
-}
-
-struct SliceInfo {
-  const void* src;
-  int tensor;   // 0 Q, 1 K, 2 V
-  int local;    // (b*H + h) within its tensor
+template <int D, bool BF16>
+struct FlowCfg {
+  static constexpr int ES = BF16 ? 2 : 4;
+  static constexpr int ROW_BYTES = D * ES;
+  static constexpr int NB = ROW_BYTES / 128;      // 128-byte boxes per input row
+  static constexpr int SB = kTR * ROW_BYTES;      // input stage
+  static constexpr int OB = kTR * D;              // output buffer (codes)
+  static constexpr int NST0 = (225280 - 2 * kGroups * OB - 4096) / SB;
+  static constexpr int NST = NST0 > 6 ? 6 : NST0;
+  static constexpr int WORDS = BF16 ? D / 2 : D;  // 32-bit input words per row
+  static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(2 * kGroups) * OB + 16 * NST + 16 * NST +
+                                 4 * WORDS + 8 * (D / 2) + kGroups * (8 * (D / 2) + 64);
+  static_assert(NST >= 2, "pipeline depth");
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ SliceInfo slice_info(const PrepareArgs& a, int s, size_t esize) {
+struct TileMeta {
+  uint32_t kind, slice, row0, pad;
+};
+
+struct SliceRef {
+  int tensor;  // 0 Q, 1 K, 2 V
+  int local;   // (b*H + h) within its tensor
+};
+
+__device__ __forceinline__ SliceRef slice_ref(const PrepareArgs& a, int s) {
   const int nq = a.B * a.Hq, nk = a.B * a.Hkv;
-  const int64_t slice = int64_t(a.N) * a.d;
-  SliceInfo r;
+  SliceRef r;
   if (s < nq) {
-    r.tensor = 0; r.local = s; r.src = static_cast<const char*>(a.Q) + esize * slice * s;
+    r.tensor = 0; r.local = s;
   } else if (s < nq + nk) {
-    r.tensor = 1; r.local = s - nq; r.src = static_cast<const char*>(a.K) + esize * slice * (s - nq);
+    r.tensor = 1; r.local = s - nq;
   } else {
-    r.tensor = 2; r.local = s - nq - nk; r.src = static_cast<const char*>(a.V) + esize * slice * (s - nq - nk);
+    r.tensor = 2; r.local = s - nq - nk;
   }
   return r;
 }
 
-// ---- mean key: fixed order (128-token chunks in token order, then chunks in order)
-template <bool BF16>
-__global__ void k_mean_partial(PrepareArgs a, int nchunks) {
-  const int chunk = blockIdx.x, bg = blockIdx.y, c = threadIdx.x;
-  const size_t es = BF16 ? 2 : 4;
-  const void* base = static_cast<const char*>(a.K) + es * int64_t(bg) * a.N * a.d;
-  const int j0 = chunk * kMeanChunk, j1 = min(a.N, j0 + kMeanChunk);
-  float part = 0.0f;
-  for (int j = j0; j < j1; ++j) part = __fadd_rn(part, load1<BF16>(base, int64_t(j) * a.d + c));
-  a.mean_part[(int64_t(bg) * nchunks + chunk) * a.d + c] = part;
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
-__global__ void k_mean_final(PrepareArgs a, int nchunks) {
-  const int bg = blockIdx.x, c = threadIdx.x;
-  float total = 0.0f;
-  for (int k = 0; k < nchunks; ++k) total = __fadd_rn(total, a.mean_part[(int64_t(bg) * nchunks + k) * a.d + c]);
-  const float mu = __fdiv_rn(total, float(a.N));
-  a.mu[bg * a.d + c] = mu;
-  if (a.k_mean) a.k_mean[bg * a.d + c] = mu;
-}
-
-__global__ void k_zero_f32(float* p, int n) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = 0.0f;
-}
-
-// ---- pass 1: amax of the transformed slice
-template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads) k_amax(PrepareArgs a) {
-  constexpr int L = D / 8, RPB = kThreads / L;
-  const int s = blockIdx.y;
-  const SliceInfo si = slice_info(a, s, BF16 ? 2 : 4);
-  const bool rotate = a.rotate && si.tensor < 2, center = a.center && si.tensor == 1;
-  const int sub = threadIdx.x % L, rloc = threadIdx.x / L;
-  float mu[8];
-  int8_t sg[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    mu[e] = center ? a.mu[si.local * D + 8 * sub + e] : 0.0f;
-    sg[e] = rotate ? a.signs[8 * sub + e] : int8_t(1);
+// ---- per-call initialisation: counters, flags, the work list -----------------
+__global__ void k_flow_init(PrepareArgs a) {
+  const int nq = a.B * a.Hq, nk = a.B * a.Hkv, ns = nq + 2 * nk;
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    a.amax_bits[i] = 0u;
+    a.a_done[i] = 0u;
+    a.s_ready[i] = 0u;
   }
-  uint32_t mx = 0;
-  for (int base = blockIdx.x * RPB; base < a.N; base += gridDim.x * RPB) {
-    const int row = base + rloc;
-    const bool valid = row < a.N;
-    float x[8];
-    if (valid) {
-      load8<BF16>(si.src, int64_t(row) * D + 8 * sub, x);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.0f;
-    }
-    transform<D>(x, sub, center, mu, rotate, sg);
-    if (valid) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) mx = max(mx, __float_as_uint(x[e]) & 0x7FFFFFFFu);
-    }
+  for (int i = threadIdx.x; i < nk; i += blockDim.x) {
+    a.m_done[i] = 0u;
+    a.mu_ready[i] = 0u;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  __shared__ uint32_t red[kThreads / 32];
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-  __syncthreads();
+  if (!a.center && a.k_mean)
+    for (int i = threadIdx.x; i < nk * a.d; i += blockDim.x) a.k_mean[i] = 0.0f;
   if (threadIdx.x == 0) {
-    uint32_t m = 0;
-    for (int w = 0; w < kThreads / 32; ++w) m = max(m, red[w]);
-    atomicMax(&a.amax_bits[s], m);
+    // slice order: K first (their M entries lead), then V, then Q
+    auto order = [&](int t) { return t < nk ? nq + t : (t < 2 * nk ? nq + t : t - 2 * nk); };
+    uint32_t e = 0;
+    for (int t = 0; t < ns + kLagA + kLagC; ++t) {
+      const int tc = t - kLagA - kLagC, ta = t - kLagA;
+      if (tc >= 0 && tc < ns) a.entries[e++] = (KIND_C << 30) | uint32_t(order(tc));
+      if (ta >= 0 && ta < ns) a.entries[e++] = (KIND_A << 30) | uint32_t(order(ta));
+      if (a.center && t < nk) a.entries[e++] = (KIND_M << 30) | uint32_t(order(t));
+    }
+    a.ctl[CTL_TICKET] = 0u;
+    a.ctl[CTL_ABORT] = 0u;
+    a.ctl[CTL_ENTRIES] = e;
   }
 }
 
-// ---- scales: qs = 448/amax, descale = amax/448 (IEEE division)
-__global__ void k_scales(PrepareArgs a, int nslices) {
-  const int s = blockIdx.x * blockDim.x + threadIdx.x;
-  if (s >= nslices) return;
-  const uint32_t bits = a.amax_bits[s];
+struct Flow {
+  PrepareArgs a;
+  int tiles_per_slice, items_per_slice;
+};
+
+__device__ __forceinline__ void raise_abort(const PrepareArgs& a) {
+  if (atomicExch(a.ctl + CTL_ABORT, 1u) == 0u) atomicOr(a.status, DEV_TIMEOUT);
+}
+
+__device__ __forceinline__ bool aborted(const PrepareArgs& a) {
+  return *reinterpret_cast<volatile uint32_t*>(a.ctl + CTL_ABORT) != 0u;
+}
+
+// Bounded wait on an mbarrier phase (one thread).
+__device__ __forceinline__ bool bar_wait(const PrepareArgs& a, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (aborted(a) || globaltimer_ns() - t0 > a.wait_ns) return false;
+  }
+}
+
+// Bounded wait for a flag in global memory set by another CTA (one thread);
+// acquire ordering for the data published before it.
+__device__ __forceinline__ bool flag_wait(const PrepareArgs& a, const uint32_t* flag) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v) return true;
+    if (aborted(a) || globaltimer_ns() - t0 > a.wait_ns) return false;
+    __nanosleep(200);
+  }
+}
+
+__device__ __forceinline__ void flag_set(uint32_t* flag) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
+}
+
+// qs = 448/amax, descale = amax/448 (IEEE division); amax = 0 -> 1, 1.
+__device__ void publish_scale(const PrepareArgs& a, int s) {
+  const uint32_t bits = atomicOr(a.amax_bits + s, 0u);
   float qs, ds;
   if (bits >= 0x7F800000u) {  // a NaN or an infinity reached the slice
     atomicOr(a.status, DEV_NONFINITE);
@@ -197,140 +179,447 @@ __global__ void k_scales(PrepareArgs a, int nslices) {
     ds = __fdiv_rn(amax, 448.0f);
   }
   a.qs[s] = qs;
-  const int nq = a.B * a.Hq, nk = a.B * a.Hkv;
-  if (s < nq) a.q_ds[s] = ds;
-  else if (s < nq + nk) a.k_ds[s - nq] = ds;
-  else a.v_ds[s - nq - nk] = ds;
+  const SliceRef r = slice_ref(a, s);
+  (r.tensor == 0 ? a.q_ds : r.tensor == 1 ? a.k_ds : a.v_ds)[r.local] = ds;
+  __threadfence();
+  flag_set(a.s_ready + s);
 }
 
-__device__ __forceinline__ uint2 cast8(const float (&x)[8], float qs) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    w[i] = cvt_e4m3x2(__fmul_rn(x[2 * i], qs), __fmul_rn(x[2 * i + 1], qs));
-  }
-  return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
-}
-
-// ---- pass 2: transform again, scale, cast (natural [.., N, d] layout)
+// ---- producer -------------------------------------------------------------
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads) k_cast(PrepareArgs a, int skip_v) {
-  constexpr int L = D / 8, RPB = kThreads / L;
-  const int s = blockIdx.y;
-  const SliceInfo si = slice_info(a, s, BF16 ? 2 : 4);
-  if (skip_v && si.tensor == 2) return;
-  const bool rotate = a.rotate && si.tensor < 2, center = a.center && si.tensor == 1;
-  const int sub = threadIdx.x % L, rloc = threadIdx.x / L;
-  float mu[8];
-  int8_t sg[8];
+__device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8_t* stages, TileMeta* meta,
+                         uint64_t* full, uint64_t* empty) {
+  using C = FlowCfg<D, BF16>;
+  const PrepareArgs& a = f.a;
+  const uint32_t total = a.ctl[CTL_ENTRIES] * uint32_t(f.items_per_slice);
+  uint32_t n = 0;  // tiles pushed
+  bool ok = true;
+  for (;;) {
+    if (aborted(a)) { ok = false; break; }
+    const uint32_t t = atomicAdd(a.ctl + CTL_TICKET, 1u);
+    if (t >= total) break;
+    const uint32_t ent = a.entries[t / uint32_t(f.items_per_slice)];
+    const uint32_t item = t % uint32_t(f.items_per_slice);
+    const uint32_t kind = ent >> 30, s = ent & 0x3FFFFFFFu;
+    const SliceRef r = slice_ref(a, int(s));
+    const CUtensorMap* map = in_maps[r.tensor];
+    const int row_begin = int(item) * kTR * kTilesPerItem;
+    for (int tl = 0; tl < kTilesPerItem && ok; ++tl, ++n) {
+      const int row0 = row_begin + tl * kTR;
+      if (row0 >= a.N) break;
+      const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
+      if (!bar_wait(a, empty + st, ph ^ 1u)) { ok = false; break; }
+      meta[st] = TileMeta{kind, s, uint32_t(row0), 0u};
+      mbar_arrive_expect_tx(full + st, C::SB);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    mu[e] = center ? a.mu[si.local * D + 8 * sub + e] : 0.0f;
-    sg[e] = rotate ? a.signs[8 * sub + e] : int8_t(1);
+      for (int b = 0; b < C::NB; ++b)
+        tma_load_3d(stages + size_t(st) * C::SB + b * (kTR * 128), map, full + st, b * 128, row0, r.local);
+    }
+    if (!ok) break;
   }
-  const float qs = a.qs[s];
-  uint8_t* dst = (si.tensor == 0 ? a.q8 : si.tensor == 1 ? a.k8 : a.v8) + int64_t(si.local) * a.N * D;
-  for (int base = blockIdx.x * RPB; base < a.N; base += gridDim.x * RPB) {
-    const int row = base + rloc;
-    const bool valid = row < a.N;
-    float x[8];
-    if (valid) {
-      load8<BF16>(si.src, int64_t(row) * D + 8 * sub, x);
+  if (ok) {
+    // one end marker per consumer group (tiles alternate between the groups)
+    for (int g = 0; g < kGroups; ++g, ++n) {
+      const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
+      if (!bar_wait(a, empty + st, ph ^ 1u)) { ok = false; break; }
+      meta[st] = TileMeta{KIND_DONE, 0u, 0u, 0u};
+      mbar_arrive(full + st);
+    }
+  }
+  if (!ok) {
+    raise_abort(a);
+    // drain: the loads of the last NST tiles may still be in flight
+    for (uint32_t x = 0; x < uint32_t(C::NST) && x < n; ++x) {
+      const uint32_t m = n - 1 - x;
+      bar_wait(a, full + m % C::NST, (m / C::NST) & 1u);
+    }
+  }
+}
+
+// ---- consumer helpers -----------------------------------------------------
+// Byte offset of 16-byte chunk c of row r in a swizzled tile of 128-byte rows.
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return uint32_t(r * 128 + ((c ^ (r & 7)) << 4)); }
+// Same for 64-byte rows (64-byte swizzle).
+__device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)); }
+
+// Row r of an input stage as packed pairs P[j] = (x_j, x_{j+D/2}); with
+// `flip`, the sign flip is applied as a sign-bit XOR on the raw values (exact,
+// signed zeros included) - only for rows that are not centred, since the
+// flip must follow the centring.
+template <int D, bool BF16>
+__device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint32_t* smask, bool flip,
+                                         uint64_t (&P)[D / 2]) {
+  using C = FlowCfg<D, BF16>;
+  constexpr int CH = C::ROW_BYTES / 16;  // 16-byte chunks per row
+  float x[D];
+#pragma unroll
+  for (int q = 0; q < CH; ++q) {
+    const int box = q / 8, cq = q % 8;
+    uint4 u = *reinterpret_cast<const uint4*>(stage + box * (kTR * 128) + sw128(r, cq));
+    if (flip) {
+      const uint4 m = *reinterpret_cast<const uint4*>(smask + 4 * q);
+      u.x ^= m.x; u.y ^= m.y; u.z ^= m.z; u.w ^= m.w;
+    }
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if constexpr (BF16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+      for (int i = 0; i < 4; ++i) x[4 * q + i] = __uint_as_float(w[i]);
     }
-    transform<D>(x, sub, center, mu, rotate, sg);
-    if (valid) *reinterpret_cast<uint2*>(dst + int64_t(row) * D + 8 * sub) = cast8(x, qs);
+  }
+#pragma unroll
+  for (int j = 0; j < D / 2; ++j) P[j] = pack2(x[j], x[j + D / 2]);
+}
+
+// Centre (x + (-mu), one rounding), then for centred rows the sign flip
+// (a sign-bit XOR on the packed pair), then the unnormalised FWHT.  The
+// order is the method's: s * (x - mu) keeps the sign of a zero difference
+// that s*x - s*mu would lose.
+template <int D>
+__device__ __forceinline__ void transform(uint64_t (&P)[D / 2], bool center, const uint64_t* nmu,
+                                          const uint64_t* pmask, bool rotate) {
+  if (center) {
+#pragma unroll
+    for (int j = 0; j < D / 2; ++j) P[j] = fadd2(P[j], nmu[j]);
+    if (rotate) {
+#pragma unroll
+      for (int j = 0; j < D / 2; j += 2) {
+        const uint4 m = *reinterpret_cast<const uint4*>(pmask + j);
+        P[j] ^= (uint64_t(m.y) << 32) | m.x;
+        P[j + 1] ^= (uint64_t(m.w) << 32) | m.z;
+      }
+    }
+  }
+  if (rotate) {
+    const uint64_t neg1 = pack2(-1.0f, -1.0f);
+#pragma unroll
+    for (int h = 1; h < D / 2; h <<= 1) {
+#pragma unroll
+      for (int j = 0; j < D / 2; ++j) {
+        if ((j & h) == 0) {
+          const uint64_t u = P[j], v = P[j + h];
+          P[j] = fadd2(u, v);
+          P[j + h] = ffma2(v, neg1, u);  // u - v, one rounding
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < D / 2; ++j) {
+      float lo, hi;
+      unpack2(P[j], lo, hi);
+      P[j] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+    }
   }
 }
 
-// ---- V cast into the transposed layout [B, Hkv, d, ldv]; tokens N..ldv-1 get 0
+template <int D>
+__device__ __forceinline__ uint32_t row_amax_bits(const uint64_t (&P)[D / 2]) {
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int j = 0; j < D / 2; ++j) {
+    float lo, hi;
+    unpack2(P[j], lo, hi);
+    m[(2 * j) & 3] = max_nan(m[(2 * j) & 3], fabsf(lo));
+    m[(2 * j + 1) & 3] = max_nan(m[(2 * j + 1) & 3], fabsf(hi));
+  }
+  return __float_as_uint(max_nan(max_nan(m[0], m[1]), max_nan(m[2], m[3])));
+}
+
+// E4M3 codes of row values x_e * qs, e = 0..D-1, as D/4 words (byte e%4 of word e/4).
+template <int D>
+__device__ __forceinline__ void row_codes(const uint64_t (&P)[D / 2], float qs, uint32_t (&cw)[D / 4]) {
+  const uint64_t q2 = pack2(qs, qs);
+  float y[D];
+#pragma unroll
+  for (int j = 0; j < D / 2; ++j) unpack2(fmul2(P[j], q2), y[j], y[j + D / 2]);
+#pragma unroll
+  for (int k = 0; k < D / 4; ++k)
+    cw[k] = pack_b16x2(cvt_e4m3x2(y[4 * k], y[4 * k + 1]), cvt_e4m3x2(y[4 * k + 2], y[4 * k + 3]));
+}
+
+// ---- the persistent kernel ----------------------------------------------------
 template <int D, bool BF16>
-__global__ void __launch_bounds__(kThreads) k_cast_vt(PrepareArgs a) {
-  constexpr int L = D / 8, RPB = kThreads / L, TOK = 64;
-  __shared__ __align__(16) uint8_t tile[D][TOK];
-  const int bg = blockIdx.y, j0 = blockIdx.x * TOK;
-  const int sub = threadIdx.x % L, rloc = threadIdx.x / L;
-  const int s = a.B * a.Hq + a.B * a.Hkv + bg;
-  const float qs = a.qs[s];
-  const size_t es = BF16 ? 2 : 4;
-  const void* src = static_cast<const char*>(a.V) + es * int64_t(bg) * a.N * D;
-#pragma unroll
-  for (int p = 0; p < TOK / RPB; ++p) {
-    const int jl = p * RPB + rloc, j = j0 + jl;
-    float x[8];
-    if (j < a.N) {
-      load8<BF16>(src, int64_t(j) * D + 8 * sub, x);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+__global__ void __launch_bounds__(kFlowThreads, 1)
+    k_prepare(const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
+              const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_q,
+              const __grid_constant__ CUtensorMap out_k, const __grid_constant__ CUtensorMap out_v, const Flow f) {
+  using C = FlowCfg<D, BF16>;
+  const PrepareArgs& a = f.a;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = sm;
+  uint8_t* outb = stages + size_t(C::NST) * C::SB;               // [group][2]
+  TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(2 * kGroups) * C::OB);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + C::NST);
+  uint64_t* empty = full + C::NST;
+  uint32_t* smask = reinterpret_cast<uint32_t*>(empty + C::NST);  // sign-bit mask per input word
+  uint64_t* pmask = reinterpret_cast<uint64_t*>(smask + C::WORDS);  // sign-bit masks of the pairs (x_j, x_{j+D/2})
+  uint8_t* gbase = reinterpret_cast<uint8_t*>(pmask + D / 2);      // per group: nmu[D/2] (8 B), 64 B scratch
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 4);  // one arrival per consumer warp
     }
-    const uint2 c = cast8(x, qs);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) tile[8 * sub + e][jl] = uint8_t(((e < 4 ? c.x : c.y) >> (8 * (e & 3))) & 0xFFu);
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < C::WORDS; i += blockDim.x) {
+    uint32_t m = 0;
+    if (a.rotate) {
+      if constexpr (BF16) {
+        m = (a.signs[2 * i] < 0 ? 0x8000u : 0u) | (a.signs[2 * i + 1] < 0 ? 0x80000000u : 0u);
+      } else {
+        m = a.signs[i] < 0 ? 0x80000000u : 0u;
+      }
+    }
+    smask[i] = m;
+  }
+  for (int j = threadIdx.x; j < D / 2; j += blockDim.x) {
+    const uint64_t lo = (a.rotate && a.signs[j] < 0) ? 0x80000000ull : 0ull;
+    const uint64_t hi = (a.rotate && a.signs[j + D / 2] < 0) ? 0x80000000ull : 0ull;
+    pmask[j] = lo | (hi << 32);
   }
   __syncthreads();
-  uint8_t* dst = a.v8 + int64_t(bg) * D * a.ldv;
-  for (int q = threadIdx.x; q < D * (TOK / 16); q += kThreads) {
-    const int c = q / (TOK / 16), part = q % (TOK / 16);
-    const int64_t j = int64_t(j0) + 16 * part;
-    if (j < a.ldv) *reinterpret_cast<uint4*>(dst + int64_t(c) * a.ldv + j) = *reinterpret_cast<const uint4*>(&tile[c][16 * part]);
-  }
-}
 
-template <int D, bool BF16>
-cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
-  const int nslices = a.B * a.Hq + 2 * a.B * a.Hkv;
-  cudaError_t e = cudaMemsetAsync(a.amax_bits, 0, sizeof(uint32_t) * nslices, st);
-  if (e != cudaSuccess) return e;
-  if (a.center) {
-    const int nchunks = (a.N + kMeanChunk - 1) / kMeanChunk;
-    k_mean_partial<BF16><<<dim3(nchunks, a.B * a.Hkv), D, 0, st>>>(a, nchunks);
-    k_mean_final<<<a.B * a.Hkv, D, 0, st>>>(a, nchunks);
-  } else if (a.k_mean) {
-    const int n = a.B * a.Hkv * D;
-    k_zero_f32<<<(n + 255) / 256, 256, 0, st>>>(a.k_mean, n);
+  if (warp == 4 * kGroups) {
+    if (lane == 0) {
+      tma_prefetch_desc(&in_q);
+      tma_prefetch_desc(&in_k);
+      tma_prefetch_desc(&in_v);
+      const CUtensorMap* maps[3] = {&in_q, &in_k, &in_v};
+      producer<D, BF16>(f, maps, stages, meta, full, empty);
+    }
+    return;
   }
-  constexpr int RPB = kThreads / (D / 8);
-  const int rb = (a.N + RPB - 1) / RPB;
-  const int gx = rb < 64 ? rb : 64;
-  k_amax<D, BF16><<<dim3(gx, nslices), kThreads, 0, st>>>(a);
-  k_scales<<<(nslices + 127) / 128, 128, 0, st>>>(a, nslices);
-  k_cast<D, BF16><<<dim3(gx, nslices), kThreads, 0, st>>>(a, a.vt);
-  if (a.vt) {
-    const int tiles = int((a.ldv + 63) / 64);
-    k_cast_vt<D, BF16><<<dim3(tiles, a.B * a.Hkv), kThreads, 0, st>>>(a);
+
+  // consumer group g: tiles g, g + 2, g + 4, ... of the ring sequence
+  const int g = warp >> 2, r = threadIdx.x & 127;
+  uint64_t* nmu = reinterpret_cast<uint64_t*>(gbase + g * (8 * (D / 2) + 64));
+  uint32_t* gscr = reinterpret_cast<uint32_t*>(nmu + D / 2);  // [0..3] warp maxima, [4] verdict
+  const uint32_t gbar = 1u + uint32_t(g);
+  int mu_bg = -1;      // K slice whose -(s*mu) is in nmu
+  int qs_slice = -1;   // slice whose scale is in qs
+  float qs = 0.0f;
+  uint32_t cbuf = 0;   // output buffer parity
+  bool stored = false;
+  bool ok = true;
+  // group-uniform verdict of thread 0's wait
+  auto group_verdict = [&](bool mine) -> bool {
+    if (r == 0) gscr[4] = mine ? 1u : 0u;
+    named_bar_sync(gbar, 128);
+    const bool v = gscr[4] != 0u;
+    named_bar_sync(gbar, 128);
+    return v;
+  };
+  for (uint32_t j = 0;; ++j) {
+    const uint32_t n = 2u * j + uint32_t(g);
+    const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
+    bool got = true;
+    if (!__all_sync(0xffffffffu, mbar_try_wait(full + st, ph))) {
+      uint32_t v = 0;
+      if (lane == 0) v = bar_wait(a, full + st, ph) ? 1u : 0u;
+      got = __shfl_sync(0xffffffffu, v, 0) != 0u;
+    }
+    if (!group_verdict(got)) { ok = false; break; }
+    const TileMeta tm = meta[st];
+    if (tm.kind == KIND_DONE) break;
+    const uint8_t* stage = stages + size_t(st) * C::SB;
+    const int s = int(tm.slice);
+    const SliceRef sr = slice_ref(a, s);
+    const int row0 = int(tm.row0);
+    const bool valid = row0 + r < a.N;
+    const bool qk = sr.tensor < 2;
+    const bool rotate = a.rotate && qk, center = a.center && sr.tensor == 1;
+
+    if (tm.kind == KIND_M) {
+      // chunk sum of each channel over the tile's tokens, in token order
+      const int rows = min(kTR, a.N - row0);
+      if (r < D) {
+        const int byte = r * C::ES, box = byte / 128, cq = (byte % 128) / 16, off = byte % 16;
+        float part = 0.0f;
+        for (int t = 0; t < rows; ++t) {
+          const uint8_t* src = stage + box * (kTR * 128) + sw128(t, cq) + off;
+          const float v = BF16 ? __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(src)) << 16)
+                               : *reinterpret_cast<const float*>(src);
+          part = __fadd_rn(part, v);
+        }
+        a.mean_part[(int64_t(sr.local) * f.tiles_per_slice + row0 / kTR) * D + r] = part;
+        __threadfence();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + st);
+      named_bar_sync(gbar, 128);
+      if (r == 0) gscr[4] = (atomicAdd(a.m_done + sr.local, 1u) + 1u == uint32_t(f.tiles_per_slice)) ? 1u : 0u;
+      named_bar_sync(gbar, 128);
+      if (gscr[4]) {
+        // last chunk of this K slice: mean = (chunk sums in order) / N
+        __threadfence();
+        if (r < D) {
+          float total = 0.0f;
+          for (int k = 0; k < f.tiles_per_slice; ++k)
+            total = __fadd_rn(total, __ldcg(a.mean_part + (int64_t(sr.local) * f.tiles_per_slice + k) * D + r));
+          const float mu = __fdiv_rn(total, float(a.N));
+          a.mu[sr.local * D + r] = mu;
+          if (a.k_mean) a.k_mean[sr.local * D + r] = mu;
+        }
+        __threadfence();
+        named_bar_sync(gbar, 128);
+        if (r == 0) flag_set(a.mu_ready + sr.local);
+      }
+      named_bar_sync(gbar, 128);
+      continue;
+    }
+
+    // centred K needs the slice's mean key
+    if (center && mu_bg != sr.local) {
+      bool have = true;
+      if (r == 0) have = flag_wait(a, a.mu_ready + sr.local);
+      if (!group_verdict(have)) { ok = false; break; }
+      if (r < D / 2) nmu[r] = pack2(-__ldcg(a.mu + sr.local * D + r), -__ldcg(a.mu + sr.local * D + r + D / 2));
+      named_bar_sync(gbar, 128);
+      mu_bg = sr.local;
+    }
+
+    uint64_t P[D / 2];
+    load_row<D, BF16>(stage, r, smask, rotate && !center, P);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + st);  // the row is in registers
+    transform<D>(P, center, nmu, pmask, rotate);
+
+    if (tm.kind == KIND_A) {
+      uint32_t m = valid ? row_amax_bits<D>(P) : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) gscr[warp & 3] = m;
+      named_bar_sync(gbar, 128);
+      if (r == 0) {
+        const uint32_t mm = max(max(gscr[0], gscr[1]), max(gscr[2], gscr[3]));
+        if (mm) atomicMax(a.amax_bits + s, mm);
+        __threadfence();
+        if (atomicAdd(a.a_done + s, 1u) + 1u == uint32_t(f.tiles_per_slice)) {
+          __threadfence();
+          publish_scale(a, s);
+        }
+      }
+      named_bar_sync(gbar, 128);
+      continue;
+    }
+
+    // KIND_C: the slice's scale, then codes through shared memory to TMA
+    if (qs_slice != s) {
+      bool have = true;
+      if (r == 0) have = flag_wait(a, a.s_ready + s);
+      if (!group_verdict(have)) { ok = false; break; }
+      qs = __ldcg(a.qs + s);
+      qs_slice = s;
+    }
+    uint32_t cw[D / 4];
+    row_codes<D>(P, qs, cw);
+    uint8_t* ob = outb + size_t(2 * g + cbuf) * C::OB;
+    // the store that last read this buffer (two casts ago) must be done with it
+    if (r == 0 && stored) bulk_wait_read<1>();
+    named_bar_sync(gbar, 128);
+    if (sr.tensor == 2 && a.vt) {
+      // channel-major: byte (channel c, token r) of a [D][128] tile, 128-byte swizzle
+#pragma unroll
+      for (int c = 0; c < D; ++c) ob[sw128(c, r >> 4) + (r & 15)] = uint8_t((cw[c >> 2] >> (8 * (c & 3))) & 0xFFu);
+    } else if constexpr (D == 128) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(ob + sw128(r, c)) = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(ob + sw64(r, c)) = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(gbar, 128);
+    if (r == 0) {
+      if (sr.tensor == 2 && a.vt) tma_store_3d(&out_v, ob, row0, 0, sr.local);
+      else tma_store_3d(sr.tensor == 0 ? &out_q : sr.tensor == 1 ? &out_k : &out_v, ob, 0, row0, sr.local);
+      bulk_commit();
+    }
+    stored = true;
+    cbuf ^= 1u;
   }
-  return cudaGetLastError();
+  if (!ok) raise_abort(a);
+  if (r == 0 && stored) bulk_wait_all();
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+template <int D, bool BF16>
+cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
+  using C = FlowCfg<D, BF16>;
+  const int nq = a.B * a.Hq, nk = a.B * a.Hkv;
+  const uint64_t rb = uint64_t(D) * C::ES;
+  CUtensorMap in_q, in_k, in_v, out_q, out_k, out_v;
+  if (encode_tiled_3d(&in_q, a.Q, rb, a.N, nq, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_tiled_3d(&in_k, a.K, rb, a.N, nk, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_tiled_3d(&in_v, a.V, rb, a.N, nk, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const CUtensorMapSwizzle osw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (encode_tiled_3d(&out_q, a.q8, D, a.N, nq, D, uint64_t(D) * a.N, D, kTR, osw) != CUDA_SUCCESS ||
+      encode_tiled_3d(&out_k, a.k8, D, a.N, nk, D, uint64_t(D) * a.N, D, kTR, osw) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  if (a.vt) {
+    if (encode_tiled_3d(&out_v, a.v8, uint64_t(a.ldv), D, nk, uint64_t(a.ldv), uint64_t(a.ldv) * D, kTR, D,
+                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else if (encode_tiled_3d(&out_v, a.v8, D, a.N, nk, D, uint64_t(D) * a.N, D, kTR, osw) != CUDA_SUCCESS) {
+    return cudaErrorInvalidValue;
+  }
+  Flow f;
+  f.a = a;
+  f.tiles_per_slice = (a.N + kTR - 1) / kTR;
+  f.items_per_slice = (f.tiles_per_slice + kTilesPerItem - 1) / kTilesPerItem;
+  k_flow_init<<<1, 256, 0, st>>>(a);
+  auto kern = k_prepare<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+  if (e != cudaSuccess) return e;
+  const int grid = a.num_sms > 0 ? a.num_sms : 1;
+  kern<<<grid, kFlowThreads, C::SMEM, st>>>(in_q, in_k, in_v, out_q, out_k, out_v, f);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t prepare_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int center) {
-  const size_t nslices = size_t(B) * Hq + 2 * size_t(B) * Hkv;
-  size_t bytes = align256(nslices * 4) + align256(nslices * 4);
+  const size_t ns = size_t(B) * Hq + 2 * size_t(B) * Hkv, nk = size_t(B) * Hkv;
+  size_t bytes = 4 * align256(ns * 4) + 2 * align256(nk * 4) + align256(16) + align256(3 * ns * 4 + 64);
   if (center) {
-    const size_t nchunks = (size_t(N) + kMeanChunk - 1) / kMeanChunk;
-    bytes += align256(size_t(B) * Hkv * nchunks * d * 4) + align256(size_t(B) * Hkv * d * 4);
+    const size_t nchunks = (size_t(N) + kTR - 1) / kTR;
+    bytes += align256(nk * nchunks * d * 4) + align256(nk * d * 4);
   }
   return bytes;
 }
 
 void carve_prepare_workspace(PrepareArgs& a, void* ws) {
-  const size_t nslices = size_t(a.B) * a.Hq + 2 * size_t(a.B) * a.Hkv;
+  const size_t ns = size_t(a.B) * a.Hq + 2 * size_t(a.B) * a.Hkv, nk = size_t(a.B) * a.Hkv;
   char* p = static_cast<char*>(ws);
-  a.amax_bits = reinterpret_cast<uint32_t*>(p);
-  p += align256(nslices * 4);
-  a.qs = reinterpret_cast<float*>(p);
-  p += align256(nslices * 4);
+  auto take = [&](size_t bytes) {
+    char* q = p;
+    p += align256(bytes);
+    return q;
+  };
+  a.amax_bits = reinterpret_cast<uint32_t*>(take(ns * 4));
+  a.qs = reinterpret_cast<float*>(take(ns * 4));
+  a.a_done = reinterpret_cast<uint32_t*>(take(ns * 4));
+  a.s_ready = reinterpret_cast<uint32_t*>(take(ns * 4));
+  a.m_done = reinterpret_cast<uint32_t*>(take(nk * 4));
+  a.mu_ready = reinterpret_cast<uint32_t*>(take(nk * 4));
+  a.ctl = reinterpret_cast<uint32_t*>(take(16));
+  a.entries = reinterpret_cast<uint32_t*>(take(3 * ns * 4 + 64));
   if (a.center) {
-    const size_t nchunks = (size_t(a.N) + kMeanChunk - 1) / kMeanChunk;
-    a.mean_part = reinterpret_cast<float*>(p);
-    p += align256(size_t(a.B) * a.Hkv * nchunks * a.d * 4);
-    a.mu = reinterpret_cast<float*>(p);
+    const size_t nchunks = (size_t(a.N) + kTR - 1) / kTR;
+    a.mean_part = reinterpret_cast<float*>(take(nk * nchunks * a.d * 4));
+    a.mu = reinterpret_cast<float*>(take(nk * a.d * 4));
   } else {
     a.mean_part = nullptr;
     a.mu = nullptr;
