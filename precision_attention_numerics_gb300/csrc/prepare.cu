@@ -23,7 +23,8 @@
 // it needs no co-residency.
 //
 // CTA: warp 8 claims items and streams their tiles into a ring of shared
-// memory stages with TMA (128-byte swizzle, rows beyond N read as zero);
+// memory stages with TMA (128-byte swizzle, rows beyond N read as zero;
+// warps 9-11 only complete its warpgroup for the register split);
 // warps 0-3 and 4-7 are two consumer groups that take alternate tiles, one
 // row per thread.  A row of d values is held as d/2 packed pairs
 // (x_j, x_{j+d/2}), so stages h = 1 .. d/4 of the FWHT are packed f32x2
@@ -41,9 +42,15 @@ namespace attnq {
 namespace {
 
 constexpr int kTR = 128;           // rows per tile = tokens per mean-key chunk
-constexpr int kTilesPerItem = 4;   // tiles per claimed item
+constexpr int kTilesPerItem = 16;  // tiles per claimed item
 constexpr int kGroups = 2;         // consumer groups (128 threads, one row each)
-constexpr int kFlowThreads = 32 * (4 * kGroups + 1);
+constexpr int kFlowThreads = 384;  // two consumer warpgroups + a warpgroup whose warp 8 is the producer
+// Register split: launched at 168 per thread (384 x 168 = 64,512); the consumer
+// warpgroups rise to 232 (a row of 128 fp32 values and the FWHT's working set
+// fit without spilling), the producer's warpgroup drops to 40:
+// 2 x 128 x 232 + 128 x 40 = 64,512.
+constexpr uint32_t kConsumerRegs = 232, kProducerRegs = 40;
+static_assert(2 * 128 * kConsumerRegs + 128 * kProducerRegs <= kFlowThreads * 168, "register split");
 constexpr int kLagA = 4, kLagC = 3;  // list steps from a slice's M entry to its A entry, and A to C
 constexpr uint32_t KIND_M = 0u, KIND_A = 1u, KIND_C = 2u, KIND_DONE = 3u;
 constexpr uint32_t CTL_TICKET = 0, CTL_ABORT = 1, CTL_ENTRIES = 2;
@@ -65,7 +72,8 @@ struct FlowCfg {
 };
 
 struct TileMeta {
-  uint32_t kind, slice, row0, pad;
+  uint32_t kind, slice, row0;
+  uint32_t last;  // 1 on the last tile of its item that the consuming group gets
 };
 
 struct SliceRef {
@@ -204,12 +212,13 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     const SliceRef r = slice_ref(a, int(s));
     const CUtensorMap* map = in_maps[r.tensor];
     const int row_begin = int(item) * kTR * kTilesPerItem;
-    for (int tl = 0; tl < kTilesPerItem && ok; ++tl, ++n) {
+    const int nt = min(kTilesPerItem, (a.N - row_begin + kTR - 1) / kTR);
+    for (int tl = 0; tl < nt && ok; ++tl, ++n) {
       const int row0 = row_begin + tl * kTR;
-      if (row0 >= a.N) break;
       const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
       if (!bar_wait(a, empty + st, ph ^ 1u)) { ok = false; break; }
-      meta[st] = TileMeta{kind, s, uint32_t(row0), 0u};
+      // tiles alternate between the groups: tl + 2 is this group's next tile
+      meta[st] = TileMeta{kind, s, uint32_t(row0), tl + 2 >= nt ? 1u : 0u};
       mbar_arrive_expect_tx(full + st, C::SB);
 #pragma unroll
       for (int b = 0; b < C::NB; ++b)
@@ -250,30 +259,36 @@ template <int D, bool BF16>
 __device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint32_t* smask, bool flip,
                                          uint64_t (&P)[D / 2]) {
   using C = FlowCfg<D, BF16>;
-  constexpr int CH = C::ROW_BYTES / 16;  // 16-byte chunks per row
-  float x[D];
-#pragma unroll
-  for (int q = 0; q < CH; ++q) {
+  constexpr int PER = BF16 ? 8 : 4, CH = C::ROW_BYTES / 16;  // elements per chunk, chunks per row
+  // The per-chunk offsets are recomputed for every tile (an opaque copy of
+  // r % 8): hoisted out of the tile loop they would hold a register each.
+  int r7 = r & 7;
+  asm volatile("" : "+r"(r7));
+  const uint8_t* rowp = stage + r * 128;
+  auto chunk = [&](int q) -> uint4 {
     const int box = q / 8, cq = q % 8;
-    uint4 u = *reinterpret_cast<const uint4*>(stage + box * (kTR * 128) + sw128(r, cq));
+    uint4 u = *reinterpret_cast<const uint4*>(rowp + box * (kTR * 128) + ((cq ^ r7) << 4));
     if (flip) {
       const uint4 m = *reinterpret_cast<const uint4*>(smask + 4 * q);
       u.x ^= m.x; u.y ^= m.y; u.z ^= m.z; u.w ^= m.w;
     }
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-    if constexpr (BF16) {
+    return u;
+  };
+  // chunk q holds elements PER*q ..; it pairs with chunk q + CH/2 (elements + D/2)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
-        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  for (int q = 0; q < CH / 2; ++q) {
+    const uint4 ua = chunk(q), ub = chunk(q + CH / 2);
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (BF16) {
+        P[PER * q + 2 * i] = pack2(__uint_as_float(wa[i] << 16), __uint_as_float(wb[i] << 16));
+        P[PER * q + 2 * i + 1] = pack2(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(wb[i] & 0xFFFF0000u));
+      } else {
+        P[PER * q + i] = pack2(__uint_as_float(wa[i]), __uint_as_float(wb[i]));
       }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[4 * q + i] = __uint_as_float(w[i]);
     }
   }
-#pragma unroll
-  for (int j = 0; j < D / 2; ++j) P[j] = pack2(x[j], x[j + D / 2]);
 }
 
 // Centre (x + (-mu), one rounding), then for centred rows the sign flip
@@ -334,12 +349,14 @@ __device__ __forceinline__ uint32_t row_amax_bits(const uint64_t (&P)[D / 2]) {
 template <int D>
 __device__ __forceinline__ void row_codes(const uint64_t (&P)[D / 2], float qs, uint32_t (&cw)[D / 4]) {
   const uint64_t q2 = pack2(qs, qs);
-  float y[D];
 #pragma unroll
-  for (int j = 0; j < D / 2; ++j) unpack2(fmul2(P[j], q2), y[j], y[j + D / 2]);
+  for (int k = 0; k < D / 8; ++k) {
+    float lo[4], hi[4];
 #pragma unroll
-  for (int k = 0; k < D / 4; ++k)
-    cw[k] = pack_b16x2(cvt_e4m3x2(y[4 * k], y[4 * k + 1]), cvt_e4m3x2(y[4 * k + 2], y[4 * k + 3]));
+    for (int i = 0; i < 4; ++i) unpack2(fmul2(P[4 * k + i], q2), lo[i], hi[i]);
+    cw[k] = pack_b16x2(cvt_e4m3x2(lo[0], lo[1]), cvt_e4m3x2(lo[2], lo[3]));              // elements 4k ..
+    cw[k + D / 8] = pack_b16x2(cvt_e4m3x2(hi[0], hi[1]), cvt_e4m3x2(hi[2], hi[3]));      // elements D/2 + 4k ..
+  }
 }
 
 // ---- the persistent kernel ----------------------------------------------------
@@ -387,8 +404,9 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   }
   __syncthreads();
 
-  if (warp == 4 * kGroups) {
-    if (lane == 0) {
+  if (warp >= 4 * kGroups) {
+    regs_decrease<kProducerRegs>();
+    if (warp == 4 * kGroups && lane == 0) {
       tma_prefetch_desc(&in_q);
       tma_prefetch_desc(&in_k);
       tma_prefetch_desc(&in_v);
@@ -399,6 +417,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   }
 
   // consumer group g: tiles g, g + 2, g + 4, ... of the ring sequence
+  regs_increase<kConsumerRegs>();
   const int g = warp >> 2, r = threadIdx.x & 127;
   uint64_t* nmu = reinterpret_cast<uint64_t*>(gbase + g * (8 * (D / 2) + 64));
   uint32_t* gscr = reinterpret_cast<uint32_t*>(nmu + D / 2);  // [0..3] warp maxima, [4] verdict
@@ -409,6 +428,8 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   uint32_t cbuf = 0;   // output buffer parity
   bool stored = false;
   bool ok = true;
+  uint32_t run_max = 0;   // this warp's amax over the group's tiles of the current item
+  uint32_t run_tiles = 0; // tiles of the current item this group has finished
   // group-uniform verdict of thread 0's wait
   auto group_verdict = [&](bool mine) -> bool {
     if (r == 0) gscr[4] = mine ? 1u : 0u;
@@ -426,6 +447,9 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       if (lane == 0) v = bar_wait(a, full + st, ph) ? 1u : 0u;
       got = __shfl_sync(0xffffffffu, v, 0) != 0u;
     }
+    // the store that last read the output buffer a cast tile would use (two
+    // casts ago) must be done with it before the group's next barrier
+    if (got && r == 0 && stored && meta[st].kind == KIND_C) bulk_wait_read<1>();
     if (!group_verdict(got)) { ok = false; break; }
     const TileMeta tm = meta[st];
     if (tm.kind == KIND_DONE) break;
@@ -442,23 +466,36 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       const int rows = min(kTR, a.N - row0);
       if (r < D) {
         const int byte = r * C::ES, box = byte / 128, cq = (byte % 128) / 16, off = byte % 16;
+        // loads in batches of 16 (independent), then the adds in token order
         float part = 0.0f;
-        for (int t = 0; t < rows; ++t) {
-          const uint8_t* src = stage + box * (kTR * 128) + sw128(t, cq) + off;
-          const float v = BF16 ? __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(src)) << 16)
-                               : *reinterpret_cast<const float*>(src);
-          part = __fadd_rn(part, v);
+        for (int t0 = 0; t0 < rows; t0 += 16) {
+          float v[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const uint8_t* src = stage + box * (kTR * 128) + sw128(t0 + u, cq) + off;
+            v[u] = BF16 ? __uint_as_float(uint32_t(*reinterpret_cast<const uint16_t*>(src)) << 16)
+                        : *reinterpret_cast<const float*>(src);
+          }
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (t0 + u < rows) part = __fadd_rn(part, v[u]);
         }
         a.mean_part[(int64_t(sr.local) * f.tiles_per_slice + row0 / kTR) * D + r] = part;
-        __threadfence();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + st);
+      ++run_tiles;
+      if (!tm.last) continue;
+      // the group's chunks of this item are written: count them (one atomic
+      // per item), and the group that completes the slice computes its mean
+      if (r < D) __threadfence();
       named_bar_sync(gbar, 128);
-      if (r == 0) gscr[4] = (atomicAdd(a.m_done + sr.local, 1u) + 1u == uint32_t(f.tiles_per_slice)) ? 1u : 0u;
+      if (r == 0)
+        gscr[4] = (atomicAdd(a.m_done + sr.local, run_tiles) + run_tiles == uint32_t(f.tiles_per_slice)) ? 1u : 0u;
+      run_tiles = 0;
       named_bar_sync(gbar, 128);
       if (gscr[4]) {
-        // last chunk of this K slice: mean = (chunk sums in order) / N
+        // last chunks of this K slice: mean = (chunk sums in order) / N
         __threadfence();
         if (r < D) {
           float total = 0.0f;
@@ -496,18 +533,23 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       uint32_t m = valid ? row_amax_bits<D>(P) : 0u;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) gscr[warp & 3] = m;
+      run_max = max(run_max, m);
+      ++run_tiles;
+      if (!tm.last) continue;
+      // end of the group's share of the item: one max and one count per item
+      if (lane == 0) gscr[warp & 3] = run_max;
       named_bar_sync(gbar, 128);
       if (r == 0) {
         const uint32_t mm = max(max(gscr[0], gscr[1]), max(gscr[2], gscr[3]));
         if (mm) atomicMax(a.amax_bits + s, mm);
         __threadfence();
-        if (atomicAdd(a.a_done + s, 1u) + 1u == uint32_t(f.tiles_per_slice)) {
+        if (atomicAdd(a.a_done + s, run_tiles) + run_tiles == uint32_t(f.tiles_per_slice)) {
           __threadfence();
           publish_scale(a, s);
         }
       }
-      named_bar_sync(gbar, 128);
+      run_max = 0;
+      run_tiles = 0;
       continue;
     }
 
@@ -522,9 +564,6 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     uint32_t cw[D / 4];
     row_codes<D>(P, qs, cw);
     uint8_t* ob = outb + size_t(2 * g + cbuf) * C::OB;
-    // the store that last read this buffer (two casts ago) must be done with it
-    if (r == 0 && stored) bulk_wait_read<1>();
-    named_bar_sync(gbar, 128);
     if (sr.tensor == 2 && a.vt) {
       // channel-major: byte (channel c, token r) of a [D][128] tile, 128-byte swizzle
 #pragma unroll
