@@ -29,8 +29,9 @@
 // row per thread.  A row of d values is held as d/2 packed pairs
 // (x_j, x_{j+d/2}), so stages h = 1 .. d/4 of the FWHT are packed f32x2
 // adds and subtracts and stage d/2 adds the two halves of each pair.  Casts
-// go to shared memory in the 128- (or 64-) byte swizzled layout and leave by
-// TMA store; V in the transposed layout is written channel-major.
+// in the natural layout leave from registers (each thread stores its row);
+// V in the transposed layout goes channel-major through shared memory and
+// leaves by TMA store.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -248,8 +249,6 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
 // ---- consumer helpers -----------------------------------------------------
 // Byte offset of 16-byte chunk c of row r in a swizzled tile of 128-byte rows.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return uint32_t(r * 128 + ((c ^ (r & 7)) << 4)); }
-// Same for 64-byte rows (64-byte swizzle).
-__device__ __forceinline__ uint32_t sw64(int r, int c) { return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4)); }
 
 // Row r of an input stage as packed pairs P[j] = (x_j, x_{j+D/2}); with
 // `flip`, the sign flip is applied as a sign-bit XOR on the raw values (exact,
@@ -363,8 +362,7 @@ __device__ __forceinline__ void row_codes(const uint64_t (&P)[D / 2], float qs, 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kFlowThreads, 1)
     k_prepare(const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
-              const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_q,
-              const __grid_constant__ CUtensorMap out_k, const __grid_constant__ CUtensorMap out_v, const Flow f) {
+              const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_vt, const Flow f) {
   using C = FlowCfg<D, BF16>;
   const PrepareArgs& a = f.a;
   extern __shared__ uint8_t smem_raw[];
@@ -449,7 +447,9 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     }
     // the store that last read the output buffer a cast tile would use (two
     // casts ago) must be done with it before the group's next barrier
-    if (got && r == 0 && stored && meta[st].kind == KIND_C) bulk_wait_read<1>();
+    if (got && r == 0 && stored && meta[st].kind == KIND_C && a.vt &&
+        slice_ref(a, int(meta[st].slice)).tensor == 2)
+      bulk_wait_read<1>();
     if (!group_verdict(got)) { ok = false; break; }
     const TileMeta tm = meta[st];
     if (tm.kind == KIND_DONE) break;
@@ -563,25 +563,25 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     }
     uint32_t cw[D / 4];
     row_codes<D>(P, qs, cw);
-    uint8_t* ob = outb + size_t(2 * g + cbuf) * C::OB;
-    if (sr.tensor == 2 && a.vt) {
-      // channel-major: byte (channel c, token r) of a [D][128] tile, 128-byte swizzle
+    if (!(sr.tensor == 2 && a.vt)) {
+      // natural layout: each thread writes its own row's codes (16-byte stores)
+      if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>((sr.tensor == 0 ? a.q8 : sr.tensor == 1 ? a.k8 : a.v8) +
+                                              (int64_t(sr.local) * a.N + row0 + r) * D);
 #pragma unroll
-      for (int c = 0; c < D; ++c) ob[sw128(c, r >> 4) + (r & 15)] = uint8_t((cw[c >> 2] >> (8 * (c & 3))) & 0xFFu);
-    } else if constexpr (D == 128) {
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(ob + sw128(r, c)) = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(ob + sw64(r, c)) = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+        for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+      }
+      continue;
     }
+    // V^T: channel-major tile through shared memory (byte (channel c, token r)
+    // of a [D][128] tile, 128-byte swizzle), then one TMA store
+    uint8_t* ob = outb + size_t(2 * g + cbuf) * C::OB;
+#pragma unroll
+    for (int c = 0; c < D; ++c) ob[sw128(c, r >> 4) + (r & 15)] = uint8_t((cw[c >> 2] >> (8 * (c & 3))) & 0xFFu);
     fence_proxy_async_smem();
     named_bar_sync(gbar, 128);
     if (r == 0) {
-      if (sr.tensor == 2 && a.vt) tma_store_3d(&out_v, ob, row0, 0, sr.local);
-      else tma_store_3d(sr.tensor == 0 ? &out_q : sr.tensor == 1 ? &out_k : &out_v, ob, 0, row0, sr.local);
+      tma_store_3d(&out_vt, ob, row0, 0, sr.local);
       bulk_commit();
     }
     stored = true;
@@ -598,21 +598,17 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   using C = FlowCfg<D, BF16>;
   const int nq = a.B * a.Hq, nk = a.B * a.Hkv;
   const uint64_t rb = uint64_t(D) * C::ES;
-  CUtensorMap in_q, in_k, in_v, out_q, out_k, out_v;
+  CUtensorMap in_q, in_k, in_v, out_vt;
   if (encode_tiled_3d(&in_q, a.Q, rb, a.N, nq, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tiled_3d(&in_k, a.K, rb, a.N, nk, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tiled_3d(&in_v, a.V, rb, a.N, nk, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const CUtensorMapSwizzle osw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if (encode_tiled_3d(&out_q, a.q8, D, a.N, nq, D, uint64_t(D) * a.N, D, kTR, osw) != CUDA_SUCCESS ||
-      encode_tiled_3d(&out_k, a.k8, D, a.N, nk, D, uint64_t(D) * a.N, D, kTR, osw) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
   if (a.vt) {
-    if (encode_tiled_3d(&out_v, a.v8, uint64_t(a.ldv), D, nk, uint64_t(a.ldv), uint64_t(a.ldv) * D, kTR, D,
+    if (encode_tiled_3d(&out_vt, a.v8, uint64_t(a.ldv), D, nk, uint64_t(a.ldv), uint64_t(a.ldv) * D, kTR, D,
                         CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  } else if (encode_tiled_3d(&out_v, a.v8, D, a.N, nk, D, uint64_t(D) * a.N, D, kTR, osw) != CUDA_SUCCESS) {
-    return cudaErrorInvalidValue;
+  } else {
+    out_vt = in_v;  // not used: casts write the natural layout from registers
   }
   Flow f;
   f.a = a;
@@ -623,7 +619,7 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
-  kern<<<grid, kFlowThreads, C::SMEM, st>>>(in_q, in_k, in_v, out_q, out_k, out_v, f);
+  kern<<<grid, kFlowThreads, C::SMEM, st>>>(in_q, in_k, in_v, out_vt, f);
   return cudaGetLastError();
 }
 
