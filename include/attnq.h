@@ -213,6 +213,18 @@ attnq_status attnq_err(const attnq_desc* desc, const void* O, int32_t o_dtype, c
  */
 attnq_status attnq_device_status(cudaStream_t stream);
 
+/*
+ * Failure-detection knob (no counterpart on the pages): every wait inside the
+ * library's kernels (on an mbarrier, or on a flag another CTA publishes) gives
+ * up after `ns` nanoseconds, records ATTNQ_ETIMEOUT in the device status word
+ * and lets the kernel finish: in-flight copies and tensor-core operations are
+ * drained with a separate one-second bound, tensor memory is freed.  With
+ * ns = 0 any wait that is not already satisfied gives up at once, which drives
+ * the timeout path without a hang.  Applies to launches made after the call
+ * (process-wide); returns the previous value.  Default 2,000,000,000 (2 s).
+ */
+uint64_t attnq_set_wait_limit_ns(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

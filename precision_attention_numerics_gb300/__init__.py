@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     attnq_prepare_static,
     ATTNQ_STATIC_SCRATCH_BYTES,
     attnq_prepare_workspace,
+    attnq_set_wait_limit_ns,
     attnq_status_string,
     attnq_version,
     attnq_vt_ld,

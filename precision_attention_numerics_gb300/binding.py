@@ -110,6 +110,8 @@ def load_library():
     L.attnq_err.argtypes = [P, P, i32, P, P, P]
     L.attnq_device_status.restype = i32
     L.attnq_device_status.argtypes = [P]
+    L.attnq_set_wait_limit_ns.restype = C.c_uint64
+    L.attnq_set_wait_limit_ns.argtypes = [C.c_uint64]
     _lib = L
     return L
 
@@ -209,3 +211,8 @@ def attnq_err(desc: AttnqDesc, O, O_ref, err_out, stream=None) -> None:
 def attnq_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the device status code (0 = OK)."""
     return int(load_library().attnq_device_status(_stream(stream)))
+
+
+def attnq_set_wait_limit_ns(ns: int) -> int:
+    """Set the limit of every wait inside the kernels (nanoseconds); returns the previous one."""
+    return int(load_library().attnq_set_wait_limit_ns(int(ns)))

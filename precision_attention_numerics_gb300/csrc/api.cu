@@ -6,8 +6,11 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "attnq.h"
 #include "internal.h"
@@ -65,7 +68,16 @@ attnq_status check_desc(const attnq_desc* d) {
 
 attnq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTNQ_OK : ATTNQ_ECUDA; }
 
-uint64_t g_wait_ns = 2000000000ull;  // 2 s per mbarrier wait
+// Host-side NVTX range around each call's launches (visible to profilers that
+// attach an NVTX tool; a no-op otherwise).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+std::atomic<uint64_t> g_wait_ns{2000000000ull};  // limit of every wait inside the kernels (2 s)
 
 }  // namespace
 
@@ -172,8 +184,9 @@ attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K,
   a.ldv = attnq_vt_ld(desc->N);
   a.status = g_status_ptr[dev];
   a.num_sms = g_num_sms[dev];
-  a.wait_ns = g_wait_ns;
+  a.wait_ns = g_wait_ns.load();
   carve_prepare_workspace(a, workspace);
+  const NvtxRange range("attnq_prepare");
   return from_cuda(launch_prepare(a, stream));
 }
 
@@ -207,8 +220,9 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
   a.ldv = attnq_vt_ld(desc->N);
   a.status = g_status_ptr[dev];
   a.num_sms = g_num_sms[dev];
-  a.wait_ns = g_wait_ns;
+  a.wait_ns = g_wait_ns.load();
   carve_prepare_workspace(a, scratch);   // the launch itself clears the counters it uses
+  const NvtxRange range("attnq_prepare");
   return from_cuda(launch_prepare(a, stream));
 }
 
@@ -241,8 +255,9 @@ attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t*
   a.underflow = reinterpret_cast<unsigned long long*>(underflow_opt);
   a.k_sink = k_sink;
   a.status = g_status_ptr[dev];
-  a.wait_ns = g_wait_ns;
+  a.wait_ns = g_wait_ns.load();
   a.num_sms = g_num_sms[dev];
+  const NvtxRange range("attnq_fwd");
   return from_cuda(launch_fwd(a, stream));
 }
 
@@ -268,6 +283,7 @@ attnq_status attnq_fwd_ponly(const attnq_desc* desc, const float* Q, const float
   a.Q = Q; a.K = K; a.V = V; a.O = O;
   a.underflow = reinterpret_cast<unsigned long long*>(underflow_opt);
   a.k_sink = k_sink;
+  const NvtxRange range("attnq_fwd_ponly");
   return from_cuda(launch_ponly(a, stream));
 }
 
@@ -287,7 +303,12 @@ attnq_status attnq_err(const attnq_desc* desc, const void* O, int32_t o_dtype, c
   a.o_bf16 = o_dtype == ATTNQ_BF16;
   a.O_ref = O_ref;
   a.err = err_out;
+  const NvtxRange range("attnq_err");
   return from_cuda(launch_err(a, stream));
+}
+
+uint64_t attnq_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_ns.exchange(ns);
 }
 
 attnq_status attnq_device_status(cudaStream_t stream) {

@@ -158,8 +158,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
                                               volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  // suspend in try_wait for at most 20 us, and never longer than the limit
+  const uint32_t hint = limit_ns < 20000ull ? uint32_t(limit_ns) : 20000u;
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }

@@ -148,10 +148,23 @@ __device__ __forceinline__ bool aborted(const PrepareArgs& a) {
 __device__ __forceinline__ bool bar_wait(const PrepareArgs& a, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
+  const uint32_t hint = a.wait_ns < 20000ull ? uint32_t(a.wait_ns) : 20000u;  // never sleep past the limit
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (aborted(a) || globaltimer_ns() - t0 > a.wait_ns) return false;
   }
+}
+
+// Bound for draining in-flight loads after an abort: independent of the wait
+// limit (which may be tiny) and of the abort flag, so no CTA leaves with a
+// copy still writing its shared memory.
+constexpr uint64_t kDrainNs = 1000000000ull;
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u))
+    if (globaltimer_ns() - t0 > kDrainNs) return;
 }
 
 // Bounded wait for a flag in global memory set by another CTA (one thread);
@@ -241,7 +254,7 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     // drain: the loads of the last NST tiles may still be in flight
     for (uint32_t x = 0; x < uint32_t(C::NST) && x < n; ++x) {
       const uint32_t m = n - 1 - x;
-      bar_wait(a, full + m % C::NST, (m / C::NST) & 1u);
+      drain_wait(full + m % C::NST, (m / C::NST) & 1u);
     }
   }
 }
