@@ -205,6 +205,38 @@ attnq_status attnq_err(const attnq_desc* desc, const void* O, int32_t o_dtype, c
                        double* err_out, cudaStream_t stream);
 
 /*
+ * FP64 reference attention ("A rounding problem, not a rotation problem",
+ * 02 / Measured heads: errors are measured against the ideal causal attention
+ * in FP64): O_ref[b,h,i] = sum_j softmax_j(q_i . k_j / sqrt(d)) v_j over
+ * j <= i (causal = 1) or all j (causal = 0), on the original inputs upcast
+ * exactly to double.  desc: B, Hq, Hkv, N, d and in_dtype are used, flags and
+ * signs are ignored.  Q, K, V: DEVICE [B,H,N,d] of in_dtype; O_ref: DEVICE fp64
+ * [B,Hq,N,d] (overwritten).  Online softmax in double; differs from a two-pass
+ * evaluation only by double rounding.  Bounded by the GPU's FP64 rate: a
+ * checking tool, not a fast path.
+ */
+attnq_status attnq_ref_attention(const attnq_desc* desc, const void* Q, const void* K, const void* V,
+                                 int32_t causal, double* O_ref, cudaStream_t stream);
+
+/*
+ * Batched four-condition report [RR, 02 / Measured heads; 03 / harm score]:
+ * for each condition c = 0 unrotated, 1 rotated, 2 centred, 3 centred and
+ * rotated, runs attnq_prepare (flags = the condition | ATTNQ_VT_LAYOUT) and
+ * attnq_fwd (causal, fp32 output) on Q, K, V and writes the per-head error
+ * against attnq_ref_attention to err_out[c * B*Hq + bh] (DEVICE fp64 [4][B*Hq]).
+ * A head's rotation harm score is err[1] - err[0] (the pages average it over
+ * the batch, their "texts").  desc->signs (DEVICE, d entries of +-1) is
+ * required; desc->flags is ignored.  workspace: DEVICE, 256-byte aligned, at
+ * least attnq_harm_workspace(desc) bytes (it holds the fp64 reference, the
+ * fp32 output, the E4M3 operands and the prepare workspace).  Errors of any
+ * step are returned as that step returns them.
+ */
+size_t attnq_harm_workspace(const attnq_desc* desc);
+attnq_status attnq_harm_report(const attnq_desc* desc, const void* Q, const void* K, const void* V, float S,
+                               int32_t kv_order, int32_t kv_tile, void* workspace, size_t ws_bytes,
+                               double* err_out, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: ATTNQ_OK, ATTNQ_ENONFINITE or ATTNQ_ETIMEOUT (the
  * first error recorded since the last call), or ATTNQ_ECUDA when the

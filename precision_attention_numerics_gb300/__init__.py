@@ -25,10 +25,13 @@ from .binding import (  # noqa: F401
     attnq_fwd,
     attnq_fwd_ponly,
     attnq_hadamard_signs,
+    attnq_harm_report,
+    attnq_harm_workspace,
     attnq_prepare,
     attnq_prepare_static,
     ATTNQ_STATIC_SCRATCH_BYTES,
     attnq_prepare_workspace,
+    attnq_ref_attention,
     attnq_set_wait_limit_ns,
     attnq_status_string,
     attnq_version,

@@ -112,6 +112,12 @@ def load_library():
     L.attnq_device_status.argtypes = [P]
     L.attnq_set_wait_limit_ns.restype = C.c_uint64
     L.attnq_set_wait_limit_ns.argtypes = [C.c_uint64]
+    L.attnq_ref_attention.restype = i32
+    L.attnq_ref_attention.argtypes = [P, P, P, P, i32, P, P]
+    L.attnq_harm_workspace.restype = sz
+    L.attnq_harm_workspace.argtypes = [P]
+    L.attnq_harm_report.restype = i32
+    L.attnq_harm_report.argtypes = [P, P, P, P, f32, i32, i32, P, sz, P, P]
     _lib = L
     return L
 
@@ -211,6 +217,27 @@ def attnq_err(desc: AttnqDesc, O, O_ref, err_out, stream=None) -> None:
 def attnq_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the device status code (0 = OK)."""
     return int(load_library().attnq_device_status(_stream(stream)))
+
+
+def attnq_ref_attention(desc: AttnqDesc, Q, K, V, causal: bool, O_ref, stream=None) -> None:
+    """FP64 reference attention of the original inputs into O_ref (fp64 [B,Hq,N,d])."""
+    d = desc._c()
+    _check(load_library().attnq_ref_attention(C.byref(d), _ptr(Q), _ptr(K), _ptr(V), int(bool(causal)),
+                                              _ptr(O_ref), _stream(stream)), "attnq_ref_attention")
+
+
+def attnq_harm_workspace(desc: AttnqDesc) -> int:
+    d = desc._c()
+    return int(load_library().attnq_harm_workspace(C.byref(d)))
+
+
+def attnq_harm_report(desc: AttnqDesc, Q, K, V, S: float, kv_order: int, kv_tile: int, workspace, err_out,
+                      stream=None) -> None:
+    """Per-head errors of the four conditions into err_out (fp64 [4, B*Hq])."""
+    d = desc._c()
+    _check(load_library().attnq_harm_report(C.byref(d), _ptr(Q), _ptr(K), _ptr(V), float(S), int(kv_order),
+                                            int(kv_tile), _ptr(workspace), workspace.numel(), _ptr(err_out),
+                                            _stream(stream)), "attnq_harm_report")
 
 
 def attnq_set_wait_limit_ns(ns: int) -> int:

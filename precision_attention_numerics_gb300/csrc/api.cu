@@ -78,6 +78,37 @@ struct NvtxRange {
 };
 
 std::atomic<uint64_t> g_wait_ns{2000000000ull};  // limit of every wait inside the kernels (2 s)
+// Carve-up of the harm-report workspace (every piece 256-byte aligned).
+struct HarmLayout {
+  size_t o_ref, o, q8, k8, v8, q_ds, k_ds, v_ds, k_mean, prep, total;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+HarmLayout harm_layout(const attnq_desc* d) {
+  const size_t nq = size_t(d->B) * d->Hq, nk = size_t(d->B) * d->Hkv, rows = size_t(d->N) * d->d;
+  attnq_desc full = *d;
+  full.flags = ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT;
+  HarmLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += a256(bytes);
+    return at;
+  };
+  L.o_ref = take(8 * nq * rows);
+  L.o = take(4 * nq * rows);
+  L.q8 = take(nq * rows);
+  L.k8 = take(nk * rows);
+  L.v8 = take(nk * size_t(d->d) * size_t(attnq_vt_ld(d->N)));
+  L.q_ds = take(4 * nq);
+  L.k_ds = take(4 * nk);
+  L.v_ds = take(4 * nk);
+  L.k_mean = take(4 * nk * d->d);
+  L.prep = take(attnq_prepare_workspace(&full));
+  L.total = off;
+  return L;
+}
 
 }  // namespace
 
@@ -305,6 +336,63 @@ attnq_status attnq_err(const attnq_desc* desc, const void* O, int32_t o_dtype, c
   a.err = err_out;
   const NvtxRange range("attnq_err");
   return from_cuda(launch_err(a, stream));
+}
+
+attnq_status attnq_ref_attention(const attnq_desc* desc, const void* Q, const void* K, const void* V,
+                                 int32_t causal, double* O_ref, cudaStream_t stream) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (desc->in_dtype != ATTNQ_F32 && desc->in_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  if (!Q || !K || !V || !O_ref || (causal != 0 && causal != 1)) return ATTNQ_EINVAL;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  RefArgs a{};
+  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d;
+  a.bf16 = desc->in_dtype == ATTNQ_BF16;
+  a.causal = causal;
+  a.Q = Q; a.K = K; a.V = V; a.O_ref = O_ref;
+  const NvtxRange range("attnq_ref_attention");
+  return from_cuda(launch_ref_attn(a, stream));
+}
+
+
+size_t attnq_harm_workspace(const attnq_desc* desc) {
+  if (check_desc(desc) != ATTNQ_OK) return 0;
+  return harm_layout(desc).total;
+}
+
+attnq_status attnq_harm_report(const attnq_desc* desc, const void* Q, const void* K, const void* V, float S,
+                               int32_t kv_order, int32_t kv_tile, void* workspace, size_t ws_bytes,
+                               double* err_out, cudaStream_t stream) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (!desc->signs || !err_out || !workspace) return ATTNQ_EINVAL;
+  const HarmLayout L = harm_layout(desc);
+  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTNQ_EINVAL;
+  char* w = static_cast<char*>(workspace);
+  double* O_ref = reinterpret_cast<double*>(w + L.o_ref);
+  st = attnq_ref_attention(desc, Q, K, V, 1, O_ref, stream);
+  if (st != ATTNQ_OK) return st;
+  attnq_scales sc{reinterpret_cast<float*>(w + L.q_ds), reinterpret_cast<float*>(w + L.k_ds),
+                  reinterpret_cast<float*>(w + L.v_ds), reinterpret_cast<float*>(w + L.k_mean)};
+  const uint32_t conds[4] = {0u, ATTNQ_ROTATE, ATTNQ_CENTER_K, ATTNQ_ROTATE | ATTNQ_CENTER_K};
+  const size_t nbh = size_t(desc->B) * desc->Hq;
+  for (int c = 0; c < 4; ++c) {
+    attnq_desc dc = *desc;
+    dc.flags = conds[c] | ATTNQ_VT_LAYOUT;
+    uint8_t* q8 = reinterpret_cast<uint8_t*>(w + L.q8);
+    uint8_t* k8 = reinterpret_cast<uint8_t*>(w + L.k8);
+    uint8_t* v8 = reinterpret_cast<uint8_t*>(w + L.v8);
+    st = attnq_prepare(&dc, Q, K, V, q8, k8, v8, &sc, w + L.prep, L.total - L.prep, stream);
+    if (st != ATTNQ_OK) return st;
+    float* O = reinterpret_cast<float*>(w + L.o);
+    st = attnq_fwd(&dc, q8, k8, v8, &sc, S, kv_order, 1, kv_tile, O, ATTNQ_F32, nullptr, 0, stream);
+    if (st != ATTNQ_OK) return st;
+    st = attnq_err(&dc, O, ATTNQ_F32, O_ref, err_out + c * nbh, stream);
+    if (st != ATTNQ_OK) return st;
+  }
+  return ATTNQ_OK;
 }
 
 uint64_t attnq_set_wait_limit_ns(uint64_t ns) {

@@ -97,6 +97,17 @@ struct ErrArgs {
 };
 cudaError_t launch_err(const ErrArgs& a, cudaStream_t s);
 
+// ---- FP64 reference attention ----------------------------------------------
+struct RefArgs {
+  int B, Hq, Hkv, N, d;
+  int bf16, causal;
+  const void* Q;
+  const void* K;
+  const void* V;
+  double* O_ref;
+};
+cudaError_t launch_ref_attn(const RefArgs& a, cudaStream_t s);
+
 // ---- driver entry point for tensor maps ------------------------------------
 CUresult encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                          uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
