@@ -240,6 +240,83 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------
+# the four-condition harm report (a widening row, not the timed hot path)
+# ---------------------------------------------------------------------------
+
+FP64_PEAK_TFLOPS = 1.25  # nominal dense FP64 of a GB300 (no measured figure exists)
+
+
+def run_harm(args):
+    """One Qwen-0.5B-shaped layer through attnq_harm_report: the FP64 reference
+    attention, then prepare + forward + per-head error for the four
+    conditions.  Reports the time per layer, the reference kernel's FP64 rate
+    against the nominal FP64 peak, and the oracle doing the same on one
+    (batch, KV group)."""
+    import torch
+
+    import oracle
+    import precision_attention_numerics_gb300 as aq
+    import synth
+    wl = synth.WORKLOADS["qwen05b"]
+    B, Hq, Hkv, N, d, T = wl["B"], wl["Hq"], wl["Hkv"], wl["N"], wl["d"], wl["kv_tile"]
+    q, k, v = synth.qwen_like_inputs(3000, B, Hq, Hkv, N, d, key_norm=wl["key_norm"],
+                                     key_channels=wl["key_channels"])
+    signs = synth.hadamard_signs(3001, d)
+    dev = torch.device("cuda")
+    Q, K, V = (torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev) for a in (q, k, v))
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, 0, torch.from_numpy(signs).to(dev))
+    ws = torch.empty(aq.attnq_harm_workspace(desc), dtype=torch.uint8, device=dev)
+    err = torch.empty((4, B * Hq), dtype=torch.float64, device=dev)
+    O_ref = torch.empty((B, Hq, N, d), dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    ms_ref = timed(lambda: aq.attnq_ref_attention(desc, Q, K, V, True, O_ref))
+    ms_rep = timed(lambda: aq.attnq_harm_report(desc, Q, K, V, 256.0, aq.ATTNQ_KV_REVERSE, T, ws, err))
+    assert aq.attnq_device_status() == 0
+    e = err.cpu().numpy()
+    harm = (e[1] - e[0]).reshape(B, Hq).mean(axis=0)
+    ref_tflops = attn_flops(B, Hq, N, d) / (ms_ref * 1e-3) / 1e12
+    # oracle: the same four conditions on batch 0, KV group 0 (its G query heads)
+    G = Hq // Hkv
+    qs, ks, vs = q[:1, :G], k[:1, :1], v[:1, :1]
+    t0 = time.perf_counter()
+    exact = oracle.attn_exact(qs, ks, vs)
+    for flags in (0, 1, 2, 3):
+        prep = oracle.prepare(qs, ks, vs, flags=flags, signs=signs)
+        emu, _ = oracle.attn_quant(prep, (1, G, 1, N, d), flags, 256.0, 1, True, T)
+        oracle.err(emu, exact)
+    dt = time.perf_counter() - t0
+    line = {"metric": "four-condition harm report, ms per Qwen-0.5B-shaped layer", "value": ms_rep, "unit": "ms",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False,
+            "vs_baseline": None, "dtype": "f64 reference + e4m3 forward", "data": "synthetic",
+            "config": {"workload": "qwen05b_layer", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "kv_tile": T,
+                       "S": 256.0, "kv_order": "reverse", "conditions": ["unrotated", "rotated", "centred",
+                                                                         "centred_rotated"]},
+            "roofline": {"kernel": "attnq_ref_attention (k_ref_attn)", "bound": "alu", "achieved": ref_tflops,
+                         "peak": FP64_PEAK_TFLOPS, "unit": "TFLOP/s fp64", "frac": ref_tflops / FP64_PEAK_TFLOPS,
+                         "traffic": None, "peak_note": "nominal dense FP64 (no measured FP64 peak)",
+                         "ms_per_launch": ms_ref},
+            "harm_mean_abs": float(np.mean(np.abs(harm))),
+            "cpu_baseline": {"value": dt * 1e3 * (B * Hkv), "unit": "ms per layer (extrapolated from one KV group)",
+                             "cores": oracle.threads(), "kind": "oracle",
+                             "sample": f"oracle exact attention + four conditions on 1 of {B * Hkv} (batch, KV group)"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
 # the CUDA path
 # ---------------------------------------------------------------------------
 
@@ -417,12 +494,16 @@ def main():
     ap.add_argument("--B", type=int, default=WL["B"], help="smaller batch for profiling captures")
     ap.add_argument("--Hq", type=int, default=WL["Hq"])
     ap.add_argument("--Hkv", type=int, default=WL["Hkv"])
+    ap.add_argument("--report", choices=["step", "harm"], default="step",
+                    help="harm: time the four-condition harm report on a Qwen-0.5B-shaped layer instead")
     args = ap.parse_args()
     WL.update(B=args.B, Hq=args.Hq, Hkv=args.Hkv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.report == "harm":
+        return run_harm(args)
     return run_ours(args)
 
 
