@@ -64,11 +64,16 @@ struct FlowCfg {
   static constexpr int SB = kTR * ROW_BYTES;      // input stage
   static constexpr int OB = kTR * D;              // output buffer (codes)
   static constexpr int NST0 = (225280 - 2 * kGroups * OB - 4096) / SB;
-  static constexpr int NST = NST0 > 6 ? 6 : NST0;
+  // A multiple of kGroups: tile n goes to stage n % NST and to group
+  // n % kGroups, so every stage serves one group only and its phases are
+  // consumed in order.  A stage shared by two groups would let a group whose
+  // tile is k phases ahead mistake an older phase of the same parity for it.
+  static constexpr int NST1 = NST0 > 6 ? 6 : NST0;
+  static constexpr int NST = NST1 - NST1 % kGroups;
   static constexpr int WORDS = BF16 ? D / 2 : D;  // 32-bit input words per row
   static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(2 * kGroups) * OB + 16 * NST + 16 * NST +
                                  4 * WORDS + 8 * (D / 2) + kGroups * (8 * (D / 2) + 64);
-  static_assert(NST >= 2, "pipeline depth");
+  static_assert(NST >= kGroups && NST % kGroups == 0, "pipeline depth: whole stages per group");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
