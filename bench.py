@@ -9,9 +9,10 @@ is needed between steps.
 
 Prints one JSON line (rank 0).  `value` is algorithmic attention TFLOP/s
 (4*d per unmasked (i, j) pair, summed over all ranks) over the device-timed
-step; `e2e` repeats the measurement through the same C calls with the bf16
-inputs copied from pinned host memory and the output copied back inside the
-timed region.  Under torchrun every rank runs its own independent replica
+step; `e2e` repeats the measurement through the C ABI's host-buffer pipeline
+(attnq_attention_host): every step copies its bf16 inputs in from pinned host
+memory and its output back inside the timed region, the copies of
+neighbouring steps overlapping each step's kernels.  Under torchrun every rank runs its own independent replica
 (weak scaling, no collective on the data path).
 
 --impl reference times the CPU oracle (the plain C++ implementation used by
@@ -388,30 +389,33 @@ def run_ours(args):
         raise RuntimeError(f"device status {aq.STATUS.get(st, st)} in the timed region")
     elapsed = max_over_ranks(elapsed, dist, dev)
 
-    # ---- end-to-end through the same C calls with host buffers
-    def e2e_step():
-        Q.copy_(Qh, non_blocking=True)
-        K.copy_(Kh, non_blocking=True)
-        V.copy_(Vh, non_blocking=True)
-        step()
-        Oh.copy_(O, non_blocking=True)
-
+    # ---- end-to-end through the C ABI's host-buffer pipeline: every step copies
+    # its Q, K, V in from pinned host memory and its O back out; the copies of
+    # step s+1's inputs and step s-1's output overlap step s's kernels
     e2e_elapsed = float("nan")
     if not args.no_e2e:
-        for _ in range(min(args.warmup, 2)):
-            e2e_step()
+        del bufs  # the pipeline keeps its own device buffers in its workspace
+        compute, copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        pws = torch.empty(aq.attnq_host_pipeline_workspace(desc, aq.ATTNQ_BF16), dtype=torch.uint8, device=dev)
+
+        def e2e_run(n):
+            aq.attnq_attention_host(desc, [Qh] * n, [Kh] * n, [Vh] * n, S, aq.ATTNQ_KV_REVERSE, True, T, [Oh] * n,
+                                    aq.ATTNQ_BF16, pws, compute, copy_in, copy_out)
+
+        e2e_run(min(args.warmup, 2))
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        s1.record(stream)
+        s0.record(compute)
+        e2e_run(args.steps)
+        s1.record(compute)
         torch.cuda.synchronize()
         e2e_elapsed = s0.elapsed_time(s1) / 1e3
-    if not args.no_e2e:
-        e2e_elapsed = max_over_ranks(e2e_elapsed, dist, dev)
+        st = aq.attnq_device_status(compute.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"device status {aq.STATUS.get(st, st)} in the end-to-end run")
+        del pws
     h2d = (Qh.numel() + Kh.numel() + Vh.numel()) * 2
     d2h = Oh.numel() * 2
 

@@ -237,6 +237,40 @@ attnq_status attnq_harm_report(const attnq_desc* desc, const void* Q, const void
                                double* err_out, cudaStream_t stream);
 
 /*
+ * Host-buffer pipeline over the whole path (no counterpart on the pages: the
+ * pages' prepare -> causal FP8 attention forward, "attention-numerics" method
+ * and kernel settings, run on inputs that live in host memory).  For each step
+ * i < n_steps, with the same desc, S, kv_order, causal and kv_tile:
+ *   Q_host[i], K_host[i], V_host[i] --copy--> device, attnq_prepare,
+ *   attnq_fwd --> device O --copy--> O_host[i].
+ * desc->flags must include ATTNQ_VT_LAYOUT.  Q/K/V_host[i]: HOST [B,H,N,d] of
+ * desc->in_dtype; O_host[i]: HOST [B,Hq,N,d] of out_dtype (ATTNQ_F32 or
+ * ATTNQ_BF16).  The arrays of pointers are read during the call only.  Host
+ * buffers should be page-locked (cudaHostAlloc / cudaHostRegister); pageable
+ * memory still gives the right result, but its copies do not overlap.
+ * Streams: the kernels run on `compute`, input copies on `copy_in`, output
+ * copies on `copy_out` (three distinct streams of the current device).  The
+ * workspace holds two input and two output buffers, so step i+1's inputs are
+ * copied in and step i-1's output out while step i's kernels run.  All work of
+ * the call starts after the work enqueued on `compute` before it, and the call
+ * makes `compute` wait for its last output copy: once `compute` is
+ * synchronised every O_host[i] is written.  The call returns after enqueueing.
+ * workspace: DEVICE, 256-byte aligned, at least
+ * attnq_host_pipeline_workspace(desc, out_dtype) bytes; the caller keeps it
+ * (and the host buffers) alive until `compute` has synchronised.  Argument
+ * errors (and a desc that attnq_prepare or attnq_fwd would refuse) are
+ * returned before anything is enqueued; ATTNQ_ECUDA if a copy or an event
+ * operation fails, after which part of the work may be enqueued.  Device-side
+ * conditions are reported by attnq_device_status as for the two calls.
+ */
+size_t attnq_host_pipeline_workspace(const attnq_desc* desc, int32_t out_dtype);
+attnq_status attnq_attention_host(const attnq_desc* desc, int32_t n_steps, const void* const* Q_host,
+                                  const void* const* K_host, const void* const* V_host, float S,
+                                  int32_t kv_order, int32_t causal, int32_t kv_tile, void* const* O_host,
+                                  int32_t out_dtype, void* workspace, size_t ws_bytes, cudaStream_t compute,
+                                  cudaStream_t copy_in, cudaStream_t copy_out);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: ATTNQ_OK, ATTNQ_ENONFINITE or ATTNQ_ETIMEOUT (the
  * first error recorded since the last call), or ATTNQ_ECUDA when the

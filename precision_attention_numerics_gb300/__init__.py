@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     AttnqError,
     AttnqScales,
     STATUS,
+    attnq_attention_host,
     attnq_device_status,
     attnq_err,
     attnq_fwd,
@@ -27,6 +28,7 @@ from .binding import (  # noqa: F401
     attnq_hadamard_signs,
     attnq_harm_report,
     attnq_harm_workspace,
+    attnq_host_pipeline_workspace,
     attnq_prepare,
     attnq_prepare_static,
     ATTNQ_STATIC_SCRATCH_BYTES,

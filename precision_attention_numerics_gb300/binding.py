@@ -118,6 +118,10 @@ def load_library():
     L.attnq_harm_workspace.argtypes = [P]
     L.attnq_harm_report.restype = i32
     L.attnq_harm_report.argtypes = [P, P, P, P, f32, i32, i32, P, sz, P, P]
+    L.attnq_host_pipeline_workspace.restype = sz
+    L.attnq_host_pipeline_workspace.argtypes = [P, i32]
+    L.attnq_attention_host.restype = i32
+    L.attnq_attention_host.argtypes = [P, i32, P, P, P, f32, i32, i32, i32, P, i32, P, sz, P, P, P]
     _lib = L
     return L
 
@@ -243,3 +247,25 @@ def attnq_harm_report(desc: AttnqDesc, Q, K, V, S: float, kv_order: int, kv_tile
 def attnq_set_wait_limit_ns(ns: int) -> int:
     """Set the limit of every wait inside the kernels (nanoseconds); returns the previous one."""
     return int(load_library().attnq_set_wait_limit_ns(int(ns)))
+
+
+def attnq_host_pipeline_workspace(desc: AttnqDesc, out_dtype: int) -> int:
+    d = desc._c()
+    return int(load_library().attnq_host_pipeline_workspace(C.byref(d), int(out_dtype)))
+
+
+def attnq_attention_host(desc: AttnqDesc, Q_host, K_host, V_host, S: float, kv_order: int, causal: bool,
+                         kv_tile: int, O_host, out_dtype: int, workspace, compute, copy_in, copy_out) -> None:
+    """Prepare + attention over n steps whose inputs and outputs live in host
+    memory (lists of pinned CPU tensors of equal length); see include/attnq.h.
+    `compute`, `copy_in`, `copy_out`: three torch.cuda.Stream objects."""
+    n = len(Q_host)
+    if not (len(K_host) == len(V_host) == len(O_host) == n):
+        raise ValueError("Q_host, K_host, V_host and O_host must have one entry per step")
+    arr = C.c_void_p * max(n, 1)
+    qa, ka, va, oa = (arr(*[t.data_ptr() for t in ts]) for ts in (Q_host, K_host, V_host, O_host))
+    d = desc._c()
+    _check(load_library().attnq_attention_host(
+        C.byref(d), n, qa, ka, va, float(S), int(kv_order), int(bool(causal)), int(kv_tile), oa, int(out_dtype),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(compute.cuda_stream),
+        _stream(copy_in.cuda_stream), _stream(copy_out.cuda_stream)), "attnq_attention_host")

@@ -110,6 +110,59 @@ HarmLayout harm_layout(const attnq_desc* d) {
   return L;
 }
 
+// Carve-up of the host-pipeline workspace: two input sets, the prepared
+// operands and their scales, the prepare workspace, two outputs.
+struct PipeLayout {
+  size_t in[2][3], q8, k8, v8, q_ds, k_ds, v_ds, k_mean, prep, out[2], total;
+  size_t in_bytes[3], out_bytes;
+};
+
+PipeLayout pipe_layout(const attnq_desc* d, int32_t out_dtype) {
+  const size_t nq = size_t(d->B) * d->Hq, nk = size_t(d->B) * d->Hkv, rows = size_t(d->N) * d->d;
+  const size_t es = d->in_dtype == ATTNQ_BF16 ? 2 : 4, eo = out_dtype == ATTNQ_BF16 ? 2 : 4;
+  PipeLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += a256(bytes);
+    return at;
+  };
+  L.in_bytes[0] = es * nq * rows;
+  L.in_bytes[1] = es * nk * rows;
+  L.in_bytes[2] = es * nk * rows;
+  for (int b = 0; b < 2; ++b)
+    for (int t = 0; t < 3; ++t) L.in[b][t] = take(L.in_bytes[t]);
+  L.q8 = take(nq * rows);
+  L.k8 = take(nk * rows);
+  L.v8 = take(nk * size_t(d->d) * size_t(attnq_vt_ld(d->N)));
+  L.q_ds = take(4 * nq);
+  L.k_ds = take(4 * nk);
+  L.v_ds = take(4 * nk);
+  L.k_mean = take(4 * nk * d->d);
+  L.prep = take(attnq_prepare_workspace(d));
+  L.out_bytes = eo * nq * rows;
+  for (int b = 0; b < 2; ++b) L.out[b] = take(L.out_bytes);
+  L.total = off;
+  return L;
+}
+
+// Events of one pipelined call, destroyed with it (an event still pending at
+// destruction is released by the runtime once it completes).
+struct PipeEvents {
+  cudaEvent_t ev[9] = {};
+  int made = 0;
+  cudaError_t create() {
+    for (; made < 9; ++made) {
+      const cudaError_t e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  ~PipeEvents() {
+    for (int i = 0; i < made; ++i) cudaEventDestroy(ev[i]);
+  }
+};
+
 }  // namespace
 
 namespace {
@@ -392,6 +445,85 @@ attnq_status attnq_harm_report(const attnq_desc* desc, const void* Q, const void
     st = attnq_err(&dc, O, ATTNQ_F32, O_ref, err_out + c * nbh, stream);
     if (st != ATTNQ_OK) return st;
   }
+  return ATTNQ_OK;
+}
+
+size_t attnq_host_pipeline_workspace(const attnq_desc* desc, int32_t out_dtype) {
+  if (check_desc(desc) != ATTNQ_OK) return 0;
+  if (desc->in_dtype != ATTNQ_F32 && desc->in_dtype != ATTNQ_BF16) return 0;
+  if (out_dtype != ATTNQ_F32 && out_dtype != ATTNQ_BF16) return 0;
+  return pipe_layout(desc, out_dtype).total;
+}
+
+attnq_status attnq_attention_host(const attnq_desc* desc, int32_t n_steps, const void* const* Q_host,
+                                  const void* const* K_host, const void* const* V_host, float S,
+                                  int32_t kv_order, int32_t causal, int32_t kv_tile, void* const* O_host,
+                                  int32_t out_dtype, void* workspace, size_t ws_bytes, cudaStream_t compute,
+                                  cudaStream_t copy_in, cudaStream_t copy_out) {
+  attnq_status st = check_desc(desc);
+  if (st != ATTNQ_OK) return st;
+  if (desc->in_dtype != ATTNQ_F32 && desc->in_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  if (out_dtype != ATTNQ_F32 && out_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
+  if (n_steps < 0 || (n_steps > 0 && (!Q_host || !K_host || !V_host || !O_host))) return ATTNQ_EINVAL;
+  for (int32_t i = 0; i < n_steps; ++i)
+    if (!Q_host[i] || !K_host[i] || !V_host[i] || !O_host[i]) return ATTNQ_EINVAL;
+  if (compute == copy_in || compute == copy_out || copy_in == copy_out) return ATTNQ_EINVAL;
+  // what attnq_prepare and attnq_fwd would refuse, refused before any work
+  if (!(desc->flags & ATTNQ_VT_LAYOUT)) return ATTNQ_EUNSUPPORTED;
+  if ((desc->flags & ATTNQ_ROTATE) && !desc->signs) return ATTNQ_EINVAL;
+  if (!(std::isfinite(S) && S > 0.0f && S <= 448.0f)) return ATTNQ_EINVAL;
+  if (kv_order != ATTNQ_KV_FORWARD && kv_order != ATTNQ_KV_REVERSE) return ATTNQ_EINVAL;
+  if (causal != 0 && causal != 1) return ATTNQ_EINVAL;
+  if (kv_tile != 64 && kv_tile != 128) return ATTNQ_EUNSUPPORTED;
+  const PipeLayout L = pipe_layout(desc, out_dtype);
+  if (!workspace || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTNQ_EINVAL;
+  int dev;
+  st = device_setup(&dev);
+  if (st != ATTNQ_OK) return st;
+  if (n_steps == 0) return ATTNQ_OK;
+  const NvtxRange range("attnq_attention_host");
+  PipeEvents E;
+  if (E.create() != cudaSuccess) return ATTNQ_ECUDA;
+  // ev[0 + b]: inputs of buffer b copied in; ev[2 + b]: buffer b read by its prepare;
+  // ev[4 + b]: output buffer b written; ev[6 + b]: output buffer b copied out;
+  // ev[8]: start (the work enqueued on `compute` so far)
+  cudaEvent_t* in_ready = E.ev, *in_free = E.ev + 2, *out_ready = E.ev + 4, *out_free = E.ev + 6, start = E.ev[8];
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaEventRecord(start, compute)) || !ok(cudaStreamWaitEvent(copy_in, start, 0)) ||
+      !ok(cudaStreamWaitEvent(copy_out, start, 0)))
+    return ATTNQ_ECUDA;
+  char* w = static_cast<char*>(workspace);
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(w + L.q8);
+  uint8_t* k8 = reinterpret_cast<uint8_t*>(w + L.k8);
+  uint8_t* v8 = reinterpret_cast<uint8_t*>(w + L.v8);
+  attnq_scales sc{reinterpret_cast<float*>(w + L.q_ds), reinterpret_cast<float*>(w + L.k_ds),
+                  reinterpret_cast<float*>(w + L.v_ds), reinterpret_cast<float*>(w + L.k_mean)};
+  const void* const* host_in[3] = {Q_host, K_host, V_host};
+  for (int32_t i = 0; i < n_steps; ++i) {
+    const int b = i & 1;
+    // inputs of step i into buffer b, once step i-2's prepare has read it
+    if (!ok(cudaStreamWaitEvent(copy_in, in_free[b], 0))) return ATTNQ_ECUDA;
+    for (int t = 0; t < 3; ++t)
+      if (!ok(cudaMemcpyAsync(w + L.in[b][t], host_in[t][i], L.in_bytes[t], cudaMemcpyHostToDevice, copy_in)))
+        return ATTNQ_ECUDA;
+    if (!ok(cudaEventRecord(in_ready[b], copy_in)) || !ok(cudaStreamWaitEvent(compute, in_ready[b], 0)))
+      return ATTNQ_ECUDA;
+    st = attnq_prepare(desc, w + L.in[b][0], w + L.in[b][1], w + L.in[b][2], q8, k8, v8, &sc, w + L.prep,
+                       L.total - L.prep, compute);
+    if (st != ATTNQ_OK) return st;
+    if (!ok(cudaEventRecord(in_free[b], compute))) return ATTNQ_ECUDA;
+    // output buffer b, once step i-2's output has been copied out
+    if (!ok(cudaStreamWaitEvent(compute, out_free[b], 0))) return ATTNQ_ECUDA;
+    st = attnq_fwd(desc, q8, k8, v8, &sc, S, kv_order, causal, kv_tile, w + L.out[b], out_dtype, nullptr, 0,
+                   compute);
+    if (st != ATTNQ_OK) return st;
+    if (!ok(cudaEventRecord(out_ready[b], compute)) || !ok(cudaStreamWaitEvent(copy_out, out_ready[b], 0)) ||
+        !ok(cudaMemcpyAsync(O_host[i], w + L.out[b], L.out_bytes, cudaMemcpyDeviceToHost, copy_out)) ||
+        !ok(cudaEventRecord(out_free[b], copy_out)))
+      return ATTNQ_ECUDA;
+  }
+  // `compute` waits for the last output copy
+  if (!ok(cudaStreamWaitEvent(compute, out_free[(n_steps - 1) & 1], 0))) return ATTNQ_ECUDA;
   return ATTNQ_OK;
 }
 

@@ -27,9 +27,7 @@ struct PrepareArgs {
   int64_t ldv;        // row length of transposed V
   // workspace carve-up
   uint32_t* amax_bits;  // [nslices]
-  float* qs;            // [nslices]
-  uint32_t* a_done;     // [nslices] tiles whose amax is in amax_bits
-  uint32_t* s_ready;    // [nslices] scale published
+  uint32_t* a_done;     // [nslices] warp-tiles whose amax is in amax_bits
   uint32_t* m_done;     // [B*Hkv] mean-key chunks summed
   uint32_t* mu_ready;   // [B*Hkv] mean key published
   uint32_t* ctl;        // [4] ticket, abort, number of entries

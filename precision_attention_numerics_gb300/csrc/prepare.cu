@@ -13,25 +13,29 @@
 // One persistent kernel does every pass.  The work is a list of entries, one
 // per (pass, slice), where a slice is one (batch, head) of Q, K or V and the
 // passes are M (mean-key chunk sums, K with centring), A (amax) and C (cast).
-// An entry's slice is cut into items of four 128-row tiles; CTAs claim items
+// An entry's slice is cut into items of a few 128-row tiles; CTAs claim items
 // in list order with an atomic ticket.  The list puts each slice's A entry a
 // few steps after its M entry and its C entry a few steps after its A entry,
-// so a slice's second and third reads come from L2, and a pass waits only on
-// entries claimed before it (the finisher of a slice's last A tile publishes
-// its scale; the finisher of a K slice's last M tile publishes its mean): the
-// earliest unfinished item never waits, so the kernel cannot deadlock, and
+// so a slice's second and third reads mostly come from L2, and a pass waits
+// only on entries claimed before it (C tiles wait until every A tile of their
+// slice has added its amax and count, then compute the scale themselves;
+// centred K tiles wait for the mean, published by the warp that completes the
+// slice's M tiles): the earliest unfinished item never waits, so the kernel
+// cannot deadlock, and
 // it needs no co-residency.
 //
 // CTA: warp 8 claims items and streams their tiles into a ring of shared
 // memory stages with TMA (128-byte swizzle, rows beyond N read as zero;
 // warps 9-11 only complete its warpgroup for the register split);
 // warps 0-3 and 4-7 are two consumer groups that take alternate tiles, one
-// row per thread.  A row of d values is held as d/2 packed pairs
+// row per thread.  The consumer warps run independently (each waits on the
+// stage, counts its own rows and stores them), so no barrier ties the warps
+// of a group together.  A row of d values is held as d/2 packed pairs
 // (x_j, x_{j+d/2}), so stages h = 1 .. d/4 of the FWHT are packed f32x2
-// adds and subtracts and stage d/2 adds the two halves of each pair.  Casts
-// in the natural layout leave from registers (each thread stores its row);
-// V in the transposed layout goes channel-major through shared memory and
-// leaves by TMA store.
+// adds and subtracts and stage d/2 adds the two halves of each pair (the
+// amax pass skips it: max(|a + b|, |a - b|) rounds to fl(|a| + |b|)).  Codes
+// leave through a per-warp staging buffer by TMA store: 32 rows in the
+// natural layout, or 32 tokens x d channels of V transposed.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -44,7 +48,8 @@ namespace {
 
 constexpr int kTR = 128;           // rows per tile = tokens per mean-key chunk
 constexpr int kTilesPerItem = 16;  // tiles per claimed item
-constexpr int kGroups = 2;         // consumer groups (128 threads, one row each)
+constexpr int kGroups = 2;         // consumer groups (4 warps, one row per thread)
+constexpr int kConsumerWarps = 4 * kGroups;
 constexpr int kFlowThreads = 384;  // two consumer warpgroups + a warpgroup whose warp 8 is the producer
 // Register split: launched at 168 per thread (384 x 168 = 64,512); the consumer
 // warpgroups rise to 232 (a row of 128 fp32 values and the FWHT's working set
@@ -52,7 +57,7 @@ constexpr int kFlowThreads = 384;  // two consumer warpgroups + a warpgroup whos
 // 2 x 128 x 232 + 128 x 40 = 64,512.
 constexpr uint32_t kConsumerRegs = 232, kProducerRegs = 40;
 static_assert(2 * 128 * kConsumerRegs + 128 * kProducerRegs <= kFlowThreads * 168, "register split");
-constexpr int kLagA = 4, kLagC = 3;  // list steps from a slice's M entry to its A entry, and A to C
+constexpr int kLagA = 4, kLagC = 7;  // least list steps from a K slice's M entry to its A entry; A to C
 constexpr uint32_t KIND_M = 0u, KIND_A = 1u, KIND_C = 2u, KIND_DONE = 3u;
 constexpr uint32_t CTL_TICKET = 0, CTL_ABORT = 1, CTL_ENTRIES = 2;
 
@@ -62,8 +67,8 @@ struct FlowCfg {
   static constexpr int ROW_BYTES = D * ES;
   static constexpr int NB = ROW_BYTES / 128;      // 128-byte boxes per input row
   static constexpr int SB = kTR * ROW_BYTES;      // input stage
-  static constexpr int OB = kTR * D;              // output buffer (codes)
-  static constexpr int NST0 = (225280 - 2 * kGroups * OB - 4096) / SB;
+  static constexpr int WB = 32 * D;               // a consumer warp's staging buffer (32 rows of codes)
+  static constexpr int NST0 = (225280 - 2 * kConsumerWarps * WB - 8192) / SB;
   // A multiple of kGroups: tile n goes to stage n % NST and to group
   // n % kGroups, so every stage serves one group only and its phases are
   // consumed in order.  A stage shared by two groups would let a group whose
@@ -71,8 +76,8 @@ struct FlowCfg {
   static constexpr int NST1 = NST0 > 6 ? 6 : NST0;
   static constexpr int NST = NST1 - NST1 % kGroups;
   static constexpr int WORDS = BF16 ? D / 2 : D;  // 32-bit input words per row
-  static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(2 * kGroups) * OB + 16 * NST + 16 * NST +
-                                 4 * WORDS + 8 * (D / 2) + kGroups * (8 * (D / 2) + 64);
+  static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(2 * kConsumerWarps) * WB + 16 * NST +
+                                 16 * NST + 4 * WORDS + 8 * (D / 2) + kConsumerWarps * 8 * (D / 2);
   static_assert(NST >= kGroups && NST % kGroups == 0, "pipeline depth: whole stages per group");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -112,7 +117,6 @@ __global__ void k_flow_init(PrepareArgs a) {
   for (int i = threadIdx.x; i < ns; i += blockDim.x) {
     a.amax_bits[i] = 0u;
     a.a_done[i] = 0u;
-    a.s_ready[i] = 0u;
   }
   for (int i = threadIdx.x; i < nk; i += blockDim.x) {
     a.m_done[i] = 0u;
@@ -120,19 +124,41 @@ __global__ void k_flow_init(PrepareArgs a) {
   }
   if (!a.center && a.k_mean)
     for (int i = threadIdx.x; i < nk * a.d; i += blockDim.x) a.k_mean[i] = 0.0f;
+  // Order of the slices' A entries.  Without centring: K, V, Q.  With
+  // centring the M entry of K slice j sits at step j, and the A order is the
+  // first L = min(kLagA, nk) V slices, then K and V alternating, then the
+  // last L K slices, then Q: K slice j's A entry comes at least L steps after
+  // its M entry, and the steps in between carry V work.
+  const int L = a.center ? (kLagA < nk ? kLagA : nk) : 0;
+  const int k0 = nq, v0 = nq + nk;
+  auto aorder = [&](int i) -> int {
+    if (!a.center) return i < nk ? k0 + i : (i < 2 * nk ? v0 + (i - nk) : i - 2 * nk);
+    if (i < L) return v0 + i;
+    i -= L;
+    if (i < 2 * (nk - L)) return (i & 1) ? v0 + L + (i >> 1) : k0 + (i >> 1);
+    i -= 2 * (nk - L);
+    if (i < L) return k0 + (nk - L) + i;
+    return i - L;
+  };
+  // Step t holds, in this order: C of the slice whose A entry was kLagC steps
+  // earlier, A, M.  Entries before step t: the C, A and M entries of steps
+  // 0 .. t-1, so every thread writes its steps' entries in place.
+  const int nsteps = ns + kLagC;
+  auto first = [&](int t) -> uint32_t {
+    const int c = (t < nsteps ? t : nsteps) - kLagC;
+    return uint32_t((c > 0 ? c : 0) + (t < ns ? t : ns) + (a.center ? (t < nk ? t : nk) : 0));
+  };
+  for (int t = threadIdx.x; t < nsteps; t += blockDim.x) {
+    uint32_t e = first(t);
+    const int tc = t - kLagC;
+    if (tc >= 0 && tc < ns) a.entries[e++] = (KIND_C << 30) | uint32_t(aorder(tc));
+    if (t < ns) a.entries[e++] = (KIND_A << 30) | uint32_t(aorder(t));
+    if (a.center && t < nk) a.entries[e++] = (KIND_M << 30) | uint32_t(k0 + t);
+  }
   if (threadIdx.x == 0) {
-    // slice order: K first (their M entries lead), then V, then Q
-    auto order = [&](int t) { return t < nk ? nq + t : (t < 2 * nk ? nq + t : t - 2 * nk); };
-    uint32_t e = 0;
-    for (int t = 0; t < ns + kLagA + kLagC; ++t) {
-      const int tc = t - kLagA - kLagC, ta = t - kLagA;
-      if (tc >= 0 && tc < ns) a.entries[e++] = (KIND_C << 30) | uint32_t(order(tc));
-      if (ta >= 0 && ta < ns) a.entries[e++] = (KIND_A << 30) | uint32_t(order(ta));
-      if (a.center && t < nk) a.entries[e++] = (KIND_M << 30) | uint32_t(order(t));
-    }
     a.ctl[CTL_TICKET] = 0u;
     a.ctl[CTL_ABORT] = 0u;
-    a.ctl[CTL_ENTRIES] = e;
+    a.ctl[CTL_ENTRIES] = first(nsteps);
   }
 }
 
@@ -149,14 +175,17 @@ __device__ __forceinline__ bool aborted(const PrepareArgs& a) {
   return *reinterpret_cast<volatile uint32_t*>(a.ctl + CTL_ABORT) != 0u;
 }
 
-// Bounded wait on an mbarrier phase (one thread).
+// Bounded wait on an mbarrier phase (one thread).  A suspended try_wait can
+// return long before its hint, so the abort flag (a global load) and the
+// clock are checked only every 64 polls: a waiting thread then costs its
+// sub-partition few issue slots.
 __device__ __forceinline__ bool bar_wait(const PrepareArgs& a, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   const uint32_t hint = a.wait_ns < 20000ull ? uint32_t(a.wait_ns) : 20000u;  // never sleep past the limit
-  for (;;) {
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_sleep(bar, parity, hint)) return true;
-    if (aborted(a) || globaltimer_ns() - t0 > a.wait_ns) return false;
+    if ((it & 63u) == 0u && (aborted(a) || globaltimer_ns() - t0 > a.wait_ns)) return false;
   }
 }
 
@@ -189,12 +218,10 @@ __device__ __forceinline__ void flag_set(uint32_t* flag) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
 }
 
-// qs = 448/amax, descale = amax/448 (IEEE division); amax = 0 -> 1, 1.
-__device__ void publish_scale(const PrepareArgs& a, int s) {
-  const uint32_t bits = atomicOr(a.amax_bits + s, 0u);
-  float qs, ds;
-  if (bits >= 0x7F800000u) {  // a NaN or an infinity reached the slice
-    atomicOr(a.status, DEV_NONFINITE);
+// qs = 448/amax, descale = amax/448 (IEEE division); amax = 0 -> 1, 1; a NaN
+// or an infinity in the slice gives qs = 0 and a NaN descale.
+__device__ __forceinline__ void scale_from_amax(uint32_t bits, float& qs, float& ds) {
+  if (bits >= 0x7F800000u) {
     qs = 0.0f;
     ds = __uint_as_float(0x7FC00000u);
   } else if (bits == 0u) {
@@ -205,11 +232,16 @@ __device__ void publish_scale(const PrepareArgs& a, int s) {
     qs = __fdiv_rn(448.0f, amax);
     ds = __fdiv_rn(amax, 448.0f);
   }
-  a.qs[s] = qs;
-  const SliceRef r = slice_ref(a, s);
-  (r.tensor == 0 ? a.q_ds : r.tensor == 1 ? a.k_ds : a.v_ds)[r.local] = ds;
-  __threadfence();
-  flag_set(a.s_ready + s);
+}
+
+__device__ __forceinline__ void red_max_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.max.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Count of finished tiles, with release ordering for this thread's earlier
+// writes (its red.max above all): a reader that acquires the final count sees
+// every contribution to the slice's amax.
+__device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ---- producer -------------------------------------------------------------
@@ -219,12 +251,20 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
   using C = FlowCfg<D, BF16>;
   const PrepareArgs& a = f.a;
   const uint32_t total = a.ctl[CTL_ENTRIES] * uint32_t(f.items_per_slice);
+  // A slice's data is read again by a later pass (A after M, C after A):
+  // keep it in L2 until the C pass reads it for the last time.
+  const uint64_t keep = l2_evict_last_policy(), last_use = l2_evict_first_policy();
   uint32_t n = 0;  // tiles pushed
   bool ok = true;
+  // The next ticket is claimed while the current item's last two tiles are
+  // pushed, so the claim's round trip stays off the ring.  Items are still
+  // finished in ticket order by this CTA, so the earliest unfinished item is
+  // always some CTA's current one and never waits.
+  uint32_t t = atomicAdd(a.ctl + CTL_TICKET, 1u);
   for (;;) {
     if (aborted(a)) { ok = false; break; }
-    const uint32_t t = atomicAdd(a.ctl + CTL_TICKET, 1u);
     if (t >= total) break;
+    uint32_t t_next = 0;
     const uint32_t ent = a.entries[t / uint32_t(f.items_per_slice)];
     const uint32_t item = t % uint32_t(f.items_per_slice);
     const uint32_t kind = ent >> 30, s = ent & 0x3FFFFFFFu;
@@ -233,6 +273,7 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     const int row_begin = int(item) * kTR * kTilesPerItem;
     const int nt = min(kTilesPerItem, (a.N - row_begin + kTR - 1) / kTR);
     for (int tl = 0; tl < nt && ok; ++tl, ++n) {
+      if (tl == (nt > 2 ? nt - 2 : 0)) t_next = atomicAdd(a.ctl + CTL_TICKET, 1u);
       const int row0 = row_begin + tl * kTR;
       const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
       if (!bar_wait(a, empty + st, ph ^ 1u)) { ok = false; break; }
@@ -241,9 +282,11 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
       mbar_arrive_expect_tx(full + st, C::SB);
 #pragma unroll
       for (int b = 0; b < C::NB; ++b)
-        tma_load_3d(stages + size_t(st) * C::SB + b * (kTR * 128), map, full + st, b * 128, row0, r.local);
+        tma_load_3d_hint(stages + size_t(st) * C::SB + b * (kTR * 128), map, full + st, b * 128, row0, r.local,
+                         kind == KIND_C ? last_use : keep);
     }
     if (!ok) break;
+    t = t_next;
   }
   if (ok) {
     // one end marker per consumer group (tiles alternate between the groups)
@@ -267,6 +310,61 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
 // ---- consumer helpers -----------------------------------------------------
 // Byte offset of 16-byte chunk c of row r in a swizzled tile of 128-byte rows.
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return uint32_t(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Byte offset of 16-byte chunk c of row r in a warp's staging buffer of D-byte
+// rows, in the swizzle its tensor map uses (128-byte rows: chunk ^ r % 8;
+// 64-byte rows: chunk ^ (r / 2) % 4): a warp writing one row per lane hits
+// every bank group once per eight lanes.
+template <int D>
+__device__ __forceinline__ uint32_t stage_off(int r, int c) {
+  if constexpr (D == 128) {
+    return uint32_t(r * 128 + ((c ^ (r & 7)) << 4));
+  } else {
+    return uint32_t(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+  }
+}
+
+// Bounded wait of a whole warp on an mbarrier phase: lane 0 sleeps on it, then
+// every lane tests the phase itself (each lane's own acquire).  The phase
+// cannot move on before this warp releases the stage, so the second test holds.
+__device__ __forceinline__ bool warp_bar_wait(const PrepareArgs& a, uint64_t* bar, uint32_t parity) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  uint32_t v = 0;
+  if ((threadIdx.x & 31) == 0) v = bar_wait(a, bar, parity) ? 1u : 0u;
+  if (__shfl_sync(0xffffffffu, v, 0) == 0u) return false;
+  return __all_sync(0xffffffffu, mbar_try_wait(bar, parity));
+}
+
+// Bounded wait of a whole warp for a flag set by another CTA; once lane 0 has
+// seen it, every lane reads it with acquire ordering before its own loads.
+__device__ __forceinline__ bool warp_flag_wait(const PrepareArgs& a, const uint32_t* flag) {
+  uint32_t v = 0;
+  if ((threadIdx.x & 31) == 0) v = flag_wait(a, flag) ? 1u : 0u;
+  if (__shfl_sync(0xffffffffu, v, 0) == 0u) return false;
+  uint32_t seen;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(flag) : "memory");
+  return __all_sync(0xffffffffu, seen != 0u);
+}
+
+// Bounded wait of a whole warp until a counter reaches `target` (another
+// CTA's release adds); every lane then reads it with acquire ordering.
+__device__ __forceinline__ bool warp_count_wait(const PrepareArgs& a, const uint32_t* ctr, uint32_t target) {
+  uint32_t v = 0;
+  if ((threadIdx.x & 31) == 0) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      uint32_t c;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(c) : "l"(ctr) : "memory");
+      if (c >= target) { v = 1u; break; }
+      if (aborted(a) || globaltimer_ns() - t0 > a.wait_ns) break;
+      __nanosleep(200);
+    }
+  }
+  if (__shfl_sync(0xffffffffu, v, 0) == 0u) return false;
+  uint32_t seen;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(ctr) : "memory");
+  return __all_sync(0xffffffffu, seen >= target);
+}
 
 // Row r of an input stage as packed pairs P[j] = (x_j, x_{j+D/2}); with
 // `flip`, the sign flip is applied as a sign-bit XOR on the raw values (exact,
@@ -309,12 +407,13 @@ __device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint
 }
 
 // Centre (x + (-mu), one rounding), then for centred rows the sign flip
-// (a sign-bit XOR on the packed pair), then the unnormalised FWHT.  The
-// order is the method's: s * (x - mu) keeps the sign of a zero difference
-// that s*x - s*mu would lose.
+// (a sign-bit XOR on the packed pair), then FWHT stages h = 1 .. D/4, which
+// act within each half of the row (packed adds and subtracts).  The order is
+// the method's: s * (x - mu) keeps the sign of a zero difference that
+// s*x - s*mu would lose.  The last stage (h = D/2) is left to the caller.
 template <int D>
-__device__ __forceinline__ void transform(uint64_t (&P)[D / 2], bool center, const uint64_t* nmu,
-                                          const uint64_t* pmask, bool rotate) {
+__device__ __forceinline__ void transform_stages(uint64_t (&P)[D / 2], bool center, const uint64_t* nmu,
+                                                 const uint64_t* pmask, bool rotate) {
   if (center) {
 #pragma unroll
     for (int j = 0; j < D / 2; ++j) P[j] = fadd2(P[j], nmu[j]);
@@ -340,24 +439,53 @@ __device__ __forceinline__ void transform(uint64_t (&P)[D / 2], bool center, con
         }
       }
     }
-#pragma unroll
-    for (int j = 0; j < D / 2; ++j) {
-      float lo, hi;
-      unpack2(P[j], lo, hi);
-      P[j] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
-    }
   }
 }
 
+// Last FWHT stage: (a_j, b_j) -> (a_j + b_j, a_j - b_j), i.e. elements j and j + D/2.
 template <int D>
-__device__ __forceinline__ uint32_t row_amax_bits(const uint64_t (&P)[D / 2]) {
+__device__ __forceinline__ void final_stage(uint64_t (&P)[D / 2]) {
+#pragma unroll
+  for (int j = 0; j < D / 2; ++j) {
+    float lo, hi;
+    unpack2(P[j], lo, hi);
+    P[j] = pack2(__fadd_rn(lo, hi), __fsub_rn(lo, hi));
+  }
+}
+
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// amax of a row held as values: max over |x| (NaN wins).
+template <int D>
+__device__ __forceinline__ uint32_t plain_amax_bits(const uint64_t (&P)[D / 2]) {
   float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
   for (int j = 0; j < D / 2; ++j) {
     float lo, hi;
     unpack2(P[j], lo, hi);
-    m[(2 * j) & 3] = max_nan(m[(2 * j) & 3], fabsf(lo));
-    m[(2 * j + 1) & 3] = max_nan(m[(2 * j + 1) & 3], fabsf(hi));
+    m[j & 3] = max3_nan(m[j & 3], fabsf(lo), fabsf(hi));
+  }
+  return __float_as_uint(max_nan(max_nan(m[0], m[1]), max_nan(m[2], m[3])));
+}
+
+// amax of a rotated row held before its last stage as pairs (a_j, b_j).  The
+// last stage gives fl(a + b) and fl(a - b); the larger of |a + b| and |a - b|
+// is |a| + |b|, and round-to-nearest-even is odd-symmetric and monotone, so
+// max(|fl(a + b)|, |fl(a - b)|) = fl(|a| + |b|) exactly (a NaN or an infinity
+// in either gives a NaN or an infinity, which the scale reports as non-finite).
+template <int D>
+__device__ __forceinline__ uint32_t rotated_amax_bits(const uint64_t (&P)[D / 2]) {
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int j = 0; j < D / 2; j += 2) {
+    float a0, b0, a1, b1;
+    unpack2(P[j], a0, b0);
+    unpack2(P[j + 1], a1, b1);
+    m[(j >> 1) & 3] = max3_nan(m[(j >> 1) & 3], __fadd_rn(fabsf(a0), fabsf(b0)), __fadd_rn(fabsf(a1), fabsf(b1)));
   }
   return __float_as_uint(max_nan(max_nan(m[0], m[1]), max_nan(m[2], m[3])));
 }
@@ -376,29 +504,64 @@ __device__ __forceinline__ void row_codes(const uint64_t (&P)[D / 2], float qs, 
   }
 }
 
+// Mean key of K slice `sl` from its chunk sums: per channel, the chunk sums
+// added in chunk order, then one division by N.  Lane l owns channels
+// l, l + 32, ...; the loads run eight chunks ahead of the ordered adds.
+template <int D>
+__device__ __forceinline__ void finish_mean(const PrepareArgs& a, int tiles_per_slice, int sl, int lane) {
+  constexpr int CPL = D / 32;
+  const float* base = a.mean_part + int64_t(sl) * tiles_per_slice * D + lane;
+  float tot[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) tot[i] = 0.0f;
+  int k = 0;
+  for (; k + 8 <= tiles_per_slice; k += 8) {
+    float v[8][CPL];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) v[u][i] = __ldcg(base + int64_t(k + u) * D + 32 * i);
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) tot[i] = __fadd_rn(tot[i], v[u][i]);
+  }
+  for (; k < tiles_per_slice; ++k)
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) tot[i] = __fadd_rn(tot[i], __ldcg(base + int64_t(k) * D + 32 * i));
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const float mu = __fdiv_rn(tot[i], float(a.N));
+    a.mu[sl * D + lane + 32 * i] = mu;
+    if (a.k_mean) a.k_mean[sl * D + lane + 32 * i] = mu;
+  }
+}
+
 // ---- the persistent kernel ----------------------------------------------------
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kFlowThreads, 1)
     k_prepare(const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
-              const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_vt, const Flow f) {
+              const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_q,
+              const __grid_constant__ CUtensorMap out_k, const __grid_constant__ CUtensorMap out_v,
+              const Flow f) {
   using C = FlowCfg<D, BF16>;
   const PrepareArgs& a = f.a;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = sm;
-  uint8_t* outb = stages + size_t(C::NST) * C::SB;               // [group][2]
-  TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(2 * kGroups) * C::OB);
+  uint8_t* outb = stages + size_t(C::NST) * C::SB;               // [consumer warp][2] staging buffers
+  TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(2 * kConsumerWarps) * C::WB);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + C::NST);
   uint64_t* empty = full + C::NST;
   uint32_t* smask = reinterpret_cast<uint32_t*>(empty + C::NST);  // sign-bit mask per input word
   uint64_t* pmask = reinterpret_cast<uint64_t*>(smask + C::WORDS);  // sign-bit masks of the pairs (x_j, x_{j+D/2})
-  uint8_t* gbase = reinterpret_cast<uint8_t*>(pmask + D / 2);      // per group: nmu[D/2] (8 B), 64 B scratch
+  uint64_t* nmu_all = pmask + D / 2;                               // per consumer warp: -mu as pairs [D/2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, 4);  // one arrival per consumer warp
+      mbar_init(empty + s, 4);  // one arrival per consumer warp of the stage's group
     }
     fence_mbar_init();
   }
@@ -420,9 +583,9 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   }
   __syncthreads();
 
-  if (warp >= 4 * kGroups) {
+  if (warp >= kConsumerWarps) {
     regs_decrease<kProducerRegs>();
-    if (warp == 4 * kGroups && lane == 0) {
+    if (warp == kConsumerWarps && lane == 0) {
       tma_prefetch_desc(&in_q);
       tma_prefetch_desc(&in_k);
       tma_prefetch_desc(&in_v);
@@ -432,43 +595,28 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     return;
   }
 
-  // consumer group g: tiles g, g + 2, g + 4, ... of the ring sequence
+  // Consumer warp: group g takes tiles g, g + 2, g + 4, ... of the ring, and
+  // warp w4 of the group rows 32*w4 .. 32*w4 + 31 of each.  Warps run
+  // independently: each waits on the stage itself, keeps its own counts and
+  // stores its own rows, so no barrier couples the warps of a group.
   regs_increase<kConsumerRegs>();
-  const int g = warp >> 2, r = threadIdx.x & 127;
-  uint64_t* nmu = reinterpret_cast<uint64_t*>(gbase + g * (8 * (D / 2) + 64));
-  uint32_t* gscr = reinterpret_cast<uint32_t*>(nmu + D / 2);  // [0..3] warp maxima, [4] verdict
-  const uint32_t gbar = 1u + uint32_t(g);
-  int mu_bg = -1;      // K slice whose -(s*mu) is in nmu
+  const int g = warp >> 2, w4 = warp & 3, r = threadIdx.x & 127;
+  uint64_t* nmu = nmu_all + warp * (D / 2);
+  uint8_t* obuf = outb + size_t(2 * warp) * C::WB;
+  const uint32_t tiles = uint32_t(f.tiles_per_slice);
+  int mu_slice = -1;   // K slice whose -mu is in nmu
   int qs_slice = -1;   // slice whose scale is in qs
   float qs = 0.0f;
-  uint32_t cbuf = 0;   // output buffer parity
+  uint32_t qs_bits = 0;  // the slice's amax bits
+  uint32_t cbuf = 0;   // staging buffer parity
   bool stored = false;
   bool ok = true;
-  uint32_t run_max = 0;   // this warp's amax over the group's tiles of the current item
-  uint32_t run_tiles = 0; // tiles of the current item this group has finished
-  // group-uniform verdict of thread 0's wait
-  auto group_verdict = [&](bool mine) -> bool {
-    if (r == 0) gscr[4] = mine ? 1u : 0u;
-    named_bar_sync(gbar, 128);
-    const bool v = gscr[4] != 0u;
-    named_bar_sync(gbar, 128);
-    return v;
-  };
+  uint32_t run_max = 0;    // amax bits of this lane's rows in the current item
+  uint32_t run_tiles = 0;  // tiles of the current item this warp has finished
   for (uint32_t j = 0;; ++j) {
     const uint32_t n = 2u * j + uint32_t(g);
     const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
-    bool got = true;
-    if (!__all_sync(0xffffffffu, mbar_try_wait(full + st, ph))) {
-      uint32_t v = 0;
-      if (lane == 0) v = bar_wait(a, full + st, ph) ? 1u : 0u;
-      got = __shfl_sync(0xffffffffu, v, 0) != 0u;
-    }
-    // the store that last read the output buffer a cast tile would use (two
-    // casts ago) must be done with it before the group's next barrier
-    if (got && r == 0 && stored && meta[st].kind == KIND_C && a.vt &&
-        slice_ref(a, int(meta[st].slice)).tensor == 2)
-      bulk_wait_read<1>();
-    if (!group_verdict(got)) { ok = false; break; }
+    if (!warp_bar_wait(a, full + st, ph)) { ok = false; break; }
     const TileMeta tm = meta[st];
     if (tm.kind == KIND_DONE) break;
     const uint8_t* stage = stages + size_t(st) * C::SB;
@@ -480,9 +628,11 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     const bool rotate = a.rotate && qk, center = a.center && sr.tensor == 1;
 
     if (tm.kind == KIND_M) {
-      // chunk sum of each channel over the tile's tokens, in token order
-      const int rows = min(kTR, a.N - row0);
-      if (r < D) {
+      // chunk sum of each channel over the tile's tokens, in token order:
+      // thread r owns channel r (warps past the last channel only release)
+      const bool has = 32 * w4 < D;
+      if (has) {
+        const int rows = min(kTR, a.N - row0);
         const int byte = r * C::ES, box = byte / 128, cq = (byte % 128) / 16, off = byte % 16;
         // loads in batches of 16 (independent), then the adds in token order
         float part = 0.0f;
@@ -502,111 +652,119 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + st);
+      if (!has) continue;
       ++run_tiles;
       if (!tm.last) continue;
-      // the group's chunks of this item are written: count them (one atomic
-      // per item), and the group that completes the slice computes its mean
-      if (r < D) __threadfence();
-      named_bar_sync(gbar, 128);
-      if (r == 0)
-        gscr[4] = (atomicAdd(a.m_done + sr.local, run_tiles) + run_tiles == uint32_t(f.tiles_per_slice)) ? 1u : 0u;
+      // this warp's chunks of the item are written: count them (one atomic per
+      // warp and item); the warp that completes the slice computes its mean
+      __threadfence();
+      __syncwarp();
+      uint32_t fin = 0;
+      if (lane == 0) fin = atomicAdd(a.m_done + sr.local, run_tiles) + run_tiles == tiles * uint32_t(D / 32) ? 1u : 0u;
       run_tiles = 0;
-      named_bar_sync(gbar, 128);
-      if (gscr[4]) {
-        // last chunks of this K slice: mean = (chunk sums in order) / N
+      if (__shfl_sync(0xffffffffu, fin, 0) != 0u) {
         __threadfence();
-        if (r < D) {
-          float total = 0.0f;
-          for (int k = 0; k < f.tiles_per_slice; ++k)
-            total = __fadd_rn(total, __ldcg(a.mean_part + (int64_t(sr.local) * f.tiles_per_slice + k) * D + r));
-          const float mu = __fdiv_rn(total, float(a.N));
-          a.mu[sr.local * D + r] = mu;
-          if (a.k_mean) a.k_mean[sr.local * D + r] = mu;
-        }
+        finish_mean<D>(a, f.tiles_per_slice, sr.local, lane);
         __threadfence();
-        named_bar_sync(gbar, 128);
-        if (r == 0) flag_set(a.mu_ready + sr.local);
+        __syncwarp();
+        if (lane == 0) flag_set(a.mu_ready + sr.local);
       }
-      named_bar_sync(gbar, 128);
       continue;
     }
 
     // centred K needs the slice's mean key
-    if (center && mu_bg != sr.local) {
-      bool have = true;
-      if (r == 0) have = flag_wait(a, a.mu_ready + sr.local);
-      if (!group_verdict(have)) { ok = false; break; }
-      if (r < D / 2) nmu[r] = pack2(-__ldcg(a.mu + sr.local * D + r), -__ldcg(a.mu + sr.local * D + r + D / 2));
-      named_bar_sync(gbar, 128);
-      mu_bg = sr.local;
+    if (center && mu_slice != sr.local) {
+      if (!warp_flag_wait(a, a.mu_ready + sr.local)) { ok = false; break; }
+      for (int jj = lane; jj < D / 2; jj += 32)
+        nmu[jj] = pack2(-__ldcg(a.mu + sr.local * D + jj), -__ldcg(a.mu + sr.local * D + jj + D / 2));
+      __syncwarp();
+      mu_slice = sr.local;
     }
 
     uint64_t P[D / 2];
     load_row<D, BF16>(stage, r, smask, rotate && !center, P);
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty + st);  // the row is in registers
-    transform<D>(P, center, nmu, pmask, rotate);
+    if (lane == 0) mbar_arrive(empty + st);  // the warp's rows are in registers
+    transform_stages<D>(P, center, nmu, pmask, rotate);
 
     if (tm.kind == KIND_A) {
-      uint32_t m = valid ? row_amax_bits<D>(P) : 0u;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      run_max = max(run_max, m);
+      if (valid) run_max = max(run_max, rotate ? rotated_amax_bits<D>(P) : plain_amax_bits<D>(P));
       ++run_tiles;
       if (!tm.last) continue;
-      // end of the group's share of the item: one max and one count per item
-      if (lane == 0) gscr[warp & 3] = run_max;
-      named_bar_sync(gbar, 128);
-      if (r == 0) {
-        const uint32_t mm = max(max(gscr[0], gscr[1]), max(gscr[2], gscr[3]));
-        if (mm) atomicMax(a.amax_bits + s, mm);
-        __threadfence();
-        if (atomicAdd(a.a_done + s, run_tiles) + run_tiles == uint32_t(f.tiles_per_slice)) {
-          __threadfence();
-          publish_scale(a, s);
-        }
+      // end of the warp's share of the item: one max and one count
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) run_max = max(run_max, __shfl_xor_sync(0xffffffffu, run_max, o));
+      if (lane == 0) {
+        if (run_max) red_max_relaxed(a.amax_bits + s, run_max);
+        red_add_release(a.a_done + s, run_tiles);
       }
       run_max = 0;
       run_tiles = 0;
       continue;
     }
 
-    // KIND_C: the slice's scale, then codes through shared memory to TMA
+    // KIND_C: the slice's scale, the last stage, codes, staged for a TMA store
     if (qs_slice != s) {
-      bool have = true;
-      if (r == 0) have = flag_wait(a, a.s_ready + s);
-      if (!group_verdict(have)) { ok = false; break; }
-      qs = __ldcg(a.qs + s);
+      // every A tile of the slice has added its amax (acquire on the count)
+      if (!warp_count_wait(a, a.a_done + s, tiles * 4u)) { ok = false; break; }
+      qs_bits = __ldcg(a.amax_bits + s);
+      float ds;
+      scale_from_amax(qs_bits, qs, ds);
       qs_slice = s;
     }
+    if (row0 == 0 && w4 == 0 && lane == 0) {
+      // the warp with the slice's first rows publishes its descale
+      float q2, ds;
+      scale_from_amax(qs_bits, q2, ds);
+      (sr.tensor == 0 ? a.q_ds : sr.tensor == 1 ? a.k_ds : a.v_ds)[sr.local] = ds;
+      if (qs_bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
+    }
+    if (rotate) final_stage<D>(P);
     uint32_t cw[D / 4];
     row_codes<D>(P, qs, cw);
-    if (!(sr.tensor == 2 && a.vt)) {
-      // natural layout: each thread writes its own row's codes (16-byte stores)
-      if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>((sr.tensor == 0 ? a.q8 : sr.tensor == 1 ? a.k8 : a.v8) +
-                                              (int64_t(sr.local) * a.N + row0 + r) * D);
+    const bool vt = sr.tensor == 2 && a.vt;
+    const int x0 = row0 + 32 * w4;  // the warp's first row (token)
+    if (int64_t(x0) >= (vt ? a.ldv : int64_t(a.N))) continue;  // all of the warp's rows are past the end
+    // the store that last read this buffer (two casts ago) must be done with it
+    if (stored && lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    uint8_t* ob = obuf + size_t(cbuf) * C::WB;
+    if (vt) {
+      // channel-major [D][32 tokens]: a 4 x 4 byte transpose within each quad
+      // of lanes turns word k of lane 4q + i (channels 4k .. 4k + 3 of token
+      // 4q + i) into channel 4k + i of tokens 4q .. 4q + 3, one 32-bit store
+      const int i4 = lane & 3;
 #pragma unroll
-        for (int c = 0; c < D / 16; ++c) dst[c] = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+      for (int k = 0; k < D / 4; ++k) {
+        const uint32_t w = cw[k];
+        // 16-bit halves with lane ^ 2, then bytes with lane ^ 1
+        const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w, 2);
+        const uint32_t w1 = (i4 & 2) ? __byte_perm(w, o1, 0x3276) : __byte_perm(w, o1, 0x5410);
+        const uint32_t o2 = __shfl_xor_sync(0xffffffffu, w1, 1);
+        const uint32_t w2 = (i4 & 1) ? __byte_perm(w1, o2, 0x3715) : __byte_perm(w1, o2, 0x6240);
+        *reinterpret_cast<uint32_t*>(ob + (4 * k + i4) * 32 + (lane & ~3)) = w2;
       }
-      continue;
-    }
-    // V^T: channel-major tile through shared memory (byte (channel c, token r)
-    // of a [D][128] tile, 128-byte swizzle), then one TMA store
-    uint8_t* ob = outb + size_t(2 * g + cbuf) * C::OB;
+    } else {
 #pragma unroll
-    for (int c = 0; c < D; ++c) ob[sw128(c, r >> 4) + (r & 15)] = uint8_t((cw[c >> 2] >> (8 * (c & 3))) & 0xFFu);
+      for (int c = 0; c < D / 16; ++c)
+        *reinterpret_cast<uint4*>(ob + stage_off<D>(lane, c)) = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+    }
     fence_proxy_async_smem();
-    named_bar_sync(gbar, 128);
-    if (r == 0) {
-      tma_store_3d(&out_vt, ob, row0, 0, sr.local);
+    __syncwarp();
+    if (lane == 0) {
+      const uint64_t once = l2_evict_first_policy();  // codes are written once and read by a later kernel
+      if (vt) {
+        tma_store_3d_hint(&out_v, ob, x0, 0, sr.local, once);
+      } else {
+        tma_store_3d_hint(sr.tensor == 0 ? &out_q : sr.tensor == 1 ? &out_k : &out_v, ob, 0, x0, sr.local, once);
+      }
       bulk_commit();
     }
     stored = true;
     cbuf ^= 1u;
   }
   if (!ok) raise_abort(a);
-  if (r == 0 && stored) bulk_wait_all();
+  if (lane == 0 && stored) bulk_wait_all();
 }
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -615,18 +773,23 @@ template <int D, bool BF16>
 cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   using C = FlowCfg<D, BF16>;
   const int nq = a.B * a.Hq, nk = a.B * a.Hkv;
-  const uint64_t rb = uint64_t(D) * C::ES;
-  CUtensorMap in_q, in_k, in_v, out_vt;
-  if (encode_tiled_3d(&in_q, a.Q, rb, a.N, nq, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-      encode_tiled_3d(&in_k, a.K, rb, a.N, nk, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-      encode_tiled_3d(&in_v, a.V, rb, a.N, nk, rb, rb * a.N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+  const uint64_t rb = uint64_t(D) * C::ES, N = uint64_t(a.N);
+  const CUtensorMapSwizzle swo = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap in_q, in_k, in_v, out_q, out_k, out_v;
+  if (encode_tiled_3d(&in_q, a.Q, rb, N, nq, rb, rb * N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_tiled_3d(&in_k, a.K, rb, N, nk, rb, rb * N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode_tiled_3d(&in_v, a.V, rb, N, nk, rb, rb * N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  // outputs: 32-row boxes, one per consumer warp
+  if (encode_tiled_3d(&out_q, a.q8, D, N, nq, D, D * N, D, 32, swo) != CUDA_SUCCESS ||
+      encode_tiled_3d(&out_k, a.k8, D, N, nk, D, D * N, D, 32, swo) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (a.vt) {
-    if (encode_tiled_3d(&out_vt, a.v8, uint64_t(a.ldv), D, nk, uint64_t(a.ldv), uint64_t(a.ldv) * D, kTR, D,
-                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    if (encode_tiled_3d(&out_v, a.v8, uint64_t(a.ldv), D, nk, uint64_t(a.ldv), uint64_t(a.ldv) * D, 32, D,
+                        CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   } else {
-    out_vt = in_v;  // not used: casts write the natural layout from registers
+    if (encode_tiled_3d(&out_v, a.v8, D, N, nk, D, D * N, D, 32, swo) != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   Flow f;
   f.a = a;
@@ -637,7 +800,7 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
-  kern<<<grid, kFlowThreads, C::SMEM, st>>>(in_q, in_k, in_v, out_vt, f);
+  kern<<<grid, kFlowThreads, C::SMEM, st>>>(in_q, in_k, in_v, out_q, out_k, out_v, f);
   return cudaGetLastError();
 }
 
@@ -645,7 +808,7 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
 
 size_t prepare_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int center) {
   const size_t ns = size_t(B) * Hq + 2 * size_t(B) * Hkv, nk = size_t(B) * Hkv;
-  size_t bytes = 4 * align256(ns * 4) + 2 * align256(nk * 4) + align256(16) + align256(3 * ns * 4 + 64);
+  size_t bytes = 2 * align256(ns * 4) + 2 * align256(nk * 4) + align256(16) + align256(3 * ns * 4 + 64);
   if (center) {
     const size_t nchunks = (size_t(N) + kTR - 1) / kTR;
     bytes += align256(nk * nchunks * d * 4) + align256(nk * d * 4);
@@ -662,9 +825,7 @@ void carve_prepare_workspace(PrepareArgs& a, void* ws) {
     return q;
   };
   a.amax_bits = reinterpret_cast<uint32_t*>(take(ns * 4));
-  a.qs = reinterpret_cast<float*>(take(ns * 4));
   a.a_done = reinterpret_cast<uint32_t*>(take(ns * 4));
-  a.s_ready = reinterpret_cast<uint32_t*>(take(ns * 4));
   a.m_done = reinterpret_cast<uint32_t*>(take(nk * 4));
   a.mu_ready = reinterpret_cast<uint32_t*>(take(nk * 4));
   a.ctl = reinterpret_cast<uint32_t*>(take(16));
