@@ -20,6 +20,8 @@ from . import build as _build
 
 ROTATE = 1
 CENTER_K = 2
+TILE_SCALES = 8
+SCALE_TILE = 128
 F32 = 0
 BF16 = 1
 NO_PCAST = 1
@@ -144,15 +146,18 @@ def _dtype_of(a) -> int:
 
 def prepare(q, k, v, flags: int = 0, signs=None):
     """Operand preparation. Returns dict with q8, k8, v8 (natural layout),
-    q_descale [B*Hq], k_descale, v_descale [B*Hkv], k_mean [B*Hkv*d]."""
+    q_descale [B*Hq], k_descale, v_descale [B*Hkv], k_mean [B*Hkv*d].  With
+    TILE_SCALES, q_descale and k_descale hold one descale per 128-row tile:
+    [B*Hq*ntiles] and [B*Hkv*ntiles], ntiles = ceil(N / 128)."""
     q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
     dt = _dtype_of(q)
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     if signs is not None:
         signs = np.ascontiguousarray(signs, dtype=np.int8)
+    nst = (N + SCALE_TILE - 1) // SCALE_TILE if flags & TILE_SCALES else 1
     out = dict(q8=np.empty(q.shape, np.uint8), k8=np.empty(k.shape, np.uint8), v8=np.empty(v.shape, np.uint8),
-               q_descale=np.empty(B * Hq, np.float32), k_descale=np.empty(B * Hkv, np.float32),
+               q_descale=np.empty(B * Hq * nst, np.float32), k_descale=np.empty(B * Hkv * nst, np.float32),
                v_descale=np.empty(B * Hkv, np.float32), k_mean=np.empty(B * Hkv * d, np.float32))
     rc = lib().orc_prepare(B, Hq, Hkv, N, d, dt, flags, _p(signs), _p(q), _p(k), _p(v), _p(out["q8"]),
                            _p(out["k8"]), _p(out["v8"]), _p(out["q_descale"]), _p(out["k_descale"]),

@@ -168,7 +168,10 @@ constexpr double LOG2E = 1.4426950408889634073599246810018921;  // 1/ln 2
 extern "C" {
 
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ENONFINITE = 4 };
-enum { ORC_ROTATE = 1u, ORC_CENTER_K = 2u };
+enum { ORC_ROTATE = 1u, ORC_CENTER_K = 2u, ORC_TILE_SCALES = 8u };
+// Scale tile of the per-tile variant: 128 consecutive tokens of one (batch,
+// head), aligned at token 0.
+constexpr int ORC_SCALE_TILE = 128;
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 
 void orc_set_threads(int t) { g_threads = t; }
@@ -243,9 +246,24 @@ int orc_mean_key(int N, int d, int dtype, const void* K_head, float* mu) {
   return ORC_OK;
 }
 
-// One tensor slice [N, d] of one (batch, head): transform, scale, cast.
+// qs = 448/amax and descale = amax/448 (IEEE division); amax = 0 gives 1, 1.
+static void scale_of(float amax, float* qs, float* ds) {
+  *qs = 1.0f;
+  *ds = 1.0f;
+  if (amax > 0.0f) {
+    *qs = 448.0f / amax;
+    *ds = amax / 448.0f;
+  }
+}
+
+// One tensor slice [N, d] of one (batch, head): transform, scale, cast.  With
+// `per_tile`, every ORC_SCALE_TILE-row tile gets its own maximum-based scale
+// (the emulator's per-tile scales that the "attention-numerics" page, method
+// and kernel settings, contrasts with the full-sequence API scales) and
+// descale[t] is tile t's; otherwise one scale for the slice.
 static int prepare_slice(int N, int d, int dtype, const void* X, bool rotate, const int8_t* signs,
-                         const float* mu /* or null */, uint8_t* x8, float* descale, float* transformed_out) {
+                         const float* mu /* or null */, uint8_t* x8, float* descale, float* transformed_out,
+                         bool per_tile = false) {
   std::vector<float> t(size_t(N) * d);
   bool finite = true;
   for (int j = 0; j < N; ++j) {
@@ -260,18 +278,18 @@ static int prepare_slice(int N, int d, int dtype, const void* X, bool rotate, co
     if (rotate) fwht(r, d);
   }
   if (!finite) return ORC_ENONFINITE;
-  float amax = 0.0f;
-  for (float x : t) {
+  for (float x : t)
     if (!finite_f(x)) return ORC_ENONFINITE;
-    amax = std::max(amax, std::fabs(x));
+  const int rows_per_scale = per_tile ? ORC_SCALE_TILE : N;
+  for (int j0 = 0, tile = 0; j0 < N; j0 += rows_per_scale, ++tile) {
+    const size_t i0 = size_t(j0) * d, i1 = size_t(std::min(N, j0 + rows_per_scale)) * d;
+    float amax = 0.0f;
+    for (size_t i = i0; i < i1; ++i) amax = std::max(amax, std::fabs(t[i]));
+    float qs, ds;
+    scale_of(amax, &qs, &ds);
+    descale[tile] = ds;
+    for (size_t i = i0; i < i1; ++i) x8[i] = e4m3_encode(t[i] * qs);
   }
-  float qs = 1.0f, ds = 1.0f;
-  if (amax > 0.0f) {
-    qs = 448.0f / amax;
-    ds = amax / 448.0f;
-  }
-  *descale = ds;
-  for (size_t i = 0; i < t.size(); ++i) x8[i] = e4m3_encode(t[i] * qs);
   if (transformed_out) std::memcpy(transformed_out, t.data(), t.size() * sizeof(float));
   return ORC_OK;
 }
@@ -280,10 +298,12 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
                 const void* Q, const void* K, const void* V, uint8_t* q8, uint8_t* k8, uint8_t* v8,
                 float* q_descale, float* k_descale, float* v_descale, float* k_mean) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || (d & (d - 1)) || Hq % Hkv) return ORC_EINVAL;
-  const bool rotate = flags & ORC_ROTATE, center = flags & ORC_CENTER_K;
+  const bool rotate = flags & ORC_ROTATE, center = flags & ORC_CENTER_K, tiles = flags & ORC_TILE_SCALES;
   if (rotate && !signs) return ORC_EINVAL;
   const size_t es = dtype == ORC_BF16 ? 2 : 4;
   const int64_t slice = int64_t(N) * d;
+  // descales per slice, or per scale tile of Q and K slices
+  const int64_t per = tiles ? (N + ORC_SCALE_TILE - 1) / ORC_SCALE_TILE : 1;
   std::atomic<int> status(ORC_OK);
   std::vector<float> mus(size_t(B) * Hkv * d, 0.0f);
   const int64_t nq = int64_t(B) * Hq, nk = int64_t(B) * Hkv;
@@ -291,7 +311,7 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
     int rc;
     if (u < nq) {
       rc = prepare_slice(N, d, dtype, static_cast<const char*>(Q) + es * slice * u, rotate, signs, nullptr,
-                         q8 + slice * u, q_descale + u, nullptr);
+                         q8 + slice * u, q_descale + per * u, nullptr, tiles);
     } else if (u < nq + nk) {
       int64_t g = u - nq;
       const void* Kh = static_cast<const char*>(K) + es * slice * g;
@@ -300,7 +320,7 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
         mu = &mus[size_t(g) * d];
         orc_mean_key(N, d, dtype, Kh, mu);
       }
-      rc = prepare_slice(N, d, dtype, Kh, rotate, signs, mu, k8 + slice * g, k_descale + g, nullptr);
+      rc = prepare_slice(N, d, dtype, Kh, rotate, signs, mu, k8 + slice * g, k_descale + per * g, nullptr, tiles);
     } else {
       int64_t g = u - nq - nk;
       rc = prepare_slice(N, d, dtype, static_cast<const char*>(V) + es * slice * g, false, nullptr, nullptr,
@@ -394,6 +414,7 @@ namespace {
 struct RowCtx {
   int N, d, T, causal, order, k_sink, mode;
   float c, S;
+  const float* c_tile;  // with per-tile scales: logit factor per key scale tile (c unused)
 };
 
 // Shared tile loop.  qrow: d doubles; key(j,c), val(j,c) return doubles.
@@ -414,7 +435,7 @@ void emulate_row(const RowCtx& x, int i, const double* qrow, KeyF key, ValF val,
       double s = 0.0;
       for (int c = 0; c < x.d; ++c) s += qrow[c] * key(j0 + jj, c);
       float sf = float(s);
-      t[jj] = sf * x.c;
+      t[jj] = sf * (x.c_tile ? x.c_tile[(j0 + jj) / ORC_SCALE_TILE] : x.c);
       mt = std::max(mt, t[jj]);
     }
     const float mnew = std::max(m, mt);
@@ -452,16 +473,22 @@ extern "C" {
 // c = fl32(dq * dk * (1/sqrt d) * (ROTATE ? 1/d : 1) * log2 e), evaluated in
 // double: the unnormalised FWHT on Q and K multiplies q.k by exactly d.
 // Softmax scale reading: the pages do not state it; the standard 1/sqrt(d).
+// With ORC_TILE_SCALES, q_ds and k_ds hold one descale per scale tile and c is
+// formed, in the same order, from the query row's tile and the key's tile
+// (the key tiles T divide the scale tile, so c is constant within a key tile).
 int orc_attn_quant(int B, int Hq, int Hkv, int N, int d, unsigned flags, const uint8_t* q8, const uint8_t* k8,
                    const uint8_t* v8, const float* q_ds, const float* k_ds, const float* v_ds, float S, int kv_order,
                    int causal, int T, int k_sink, int mode, const int32_t* bh_list, int n_bh, const int32_t* rows,
                    int n_rows, double* O, uint64_t* underflow /* [n_bh, 2] or null */) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || T <= 0 || Hq % Hkv || !(S > 0.0f)) return ORC_EINVAL;
+  const bool tiles = flags & ORC_TILE_SCALES;
+  if (tiles && ORC_SCALE_TILE % T) return ORC_EINVAL;
   if (!bh_list) n_bh = B * Hq;
   if (!rows) n_rows = N;
   const int group = Hq / Hkv;
   const int64_t slice = int64_t(N) * d;
   const bool rotate = flags & ORC_ROTATE;
+  const int nst = tiles ? (N + ORC_SCALE_TILE - 1) / ORC_SCALE_TILE : 1;  // descales per Q/K slice
   const int RB = 16;
   const int64_t nblk = (n_rows + RB - 1) / RB;
   std::vector<uint64_t> uf_part(size_t(n_bh) * nblk * 2, 0);
@@ -472,14 +499,23 @@ int orc_attn_quant(int B, int Hq, int Hkv, int N, int d, unsigned flags, const u
     const uint8_t* qh = q8 + (int64_t(b) * Hq + h) * slice;
     const uint8_t* kh = k8 + (int64_t(b) * Hkv + g) * slice;
     const uint8_t* vh = v8 + (int64_t(b) * Hkv + g) * slice;
-    const double cfac = double(q_ds[b * Hq + h]) * double(k_ds[b * Hkv + g]) * (1.0 / std::sqrt(double(d))) *
-                        (rotate ? 1.0 / double(d) : 1.0) * LOG2E;
-    RowCtx x{N, d, T, causal, kv_order, k_sink, mode, float(cfac), S};
+    auto logit_factor = [&](float dq, float dk) {
+      return float(double(dq) * double(dk) * (1.0 / std::sqrt(double(d))) * (rotate ? 1.0 / double(d) : 1.0) *
+                   LOG2E);
+    };
+    const float* qd = q_ds + (int64_t(b) * Hq + h) * nst;
+    const float* kd = k_ds + (int64_t(b) * Hkv + g) * nst;
+    RowCtx x{N, d, T, causal, kv_order, k_sink, mode, logit_factor(qd[0], kd[0]), S, nullptr};
+    std::vector<float> c_tile(nst);
     const double dv = double(v_ds[b * Hkv + g]);
     std::vector<double> q(d);
     std::vector<float> acc(d);
     for (int r = rb * RB; r < std::min(n_rows, rb * RB + RB); ++r) {
       int i = rows ? rows[r] : r;
+      if (tiles) {
+        for (int t = 0; t < nst; ++t) c_tile[t] = logit_factor(qd[i / ORC_SCALE_TILE], kd[t]);
+        x.c_tile = c_tile.data();
+      }
       for (int c = 0; c < d; ++c) q[c] = dec(qh[int64_t(i) * d + c]);
       float l;
       emulate_row(
@@ -523,7 +559,7 @@ int orc_attn_ponly(int B, int Hq, int Hkv, int N, int d, const float* Q, const f
     const float* qh = Q + (int64_t(b) * Hq + h) * slice;
     const float* kh = K + (int64_t(b) * Hkv + g) * slice;
     const float* vh = V + (int64_t(b) * Hkv + g) * slice;
-    RowCtx x{N, d, T, causal, kv_order, k_sink, mode, cfac, S};
+    RowCtx x{N, d, T, causal, kv_order, k_sink, mode, cfac, S, nullptr};
     std::vector<double> q(d);
     std::vector<float> acc(d);
     for (int r = rb * RB; r < std::min(n_rows, rb * RB + RB); ++r) {

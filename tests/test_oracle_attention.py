@@ -265,3 +265,51 @@ def test_round_bf16_is_nearest_even(orc):
         for nb in (lo, hi):
             dn = abs(Fraction(xi) - Fraction(float(nb)))
             assert dv < dn or (dv == dn and (g & 1) == 0)
+
+
+def test_quant_tile_scales_equal_to_slice_scales_give_slice_result(orc):
+    """The per-tile path with every tile's descale equal to the slice's is the
+    full-sequence computation, bit for bit."""
+    B, Hq, Hkv, N, d = 1, 4, 2, 300, 64
+    qb, kb, vb = synth.qwen_like_inputs(52, B, Hq, Hkv, N, d, key_norm=30.0, key_channels=4)
+    p = orc.prepare(qb, kb, vb, flags=3, signs=synth.hadamard_signs(8, d))
+    nt = 3
+    pt = dict(p)
+    pt["q_descale"] = np.repeat(p["q_descale"], nt)
+    pt["k_descale"] = np.repeat(p["k_descale"], nt)
+    for T in (64, 128):
+        a, ua = orc.attn_quant(p, (B, Hq, Hkv, N, d), 3, 256.0, 1, True, T)
+        b, ub = orc.attn_quant(pt, (B, Hq, Hkv, N, d), 3 | orc.TILE_SCALES, 256.0, 1, True, T)
+        assert np.array_equal(a, b) and np.array_equal(ua, ub)
+
+
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quant_tile_scales_without_pcast_is_sdpa_on_dequantised_operands(orc, rotate):
+    """Per-tile descales applied to the right query and key tiles: with the P cast off
+    the emulation is exact attention on the operands dequantised tile by tile."""
+    B, Hq, Hkv, N, d, TS = 1, 4, 2, 330, 64, 128
+    nt = (N + TS - 1) // TS
+    qb, kb, vb = synth.qwen_like_inputs(53, B, Hq, Hkv, N, d, key_norm=30.0, key_channels=4)
+    # make the tiles' scales differ a lot
+    for x in (qb, kb):
+        f = synth.bf16_bits_to_f32(x)
+        f[:, :, 128:256] *= 8.0
+        f[:, :, 256:] *= 0.125
+        x[...] = orc.round_bf16(f.astype(np.float64))
+    flags = (1 if rotate else 0) | 2 | orc.TILE_SCALES
+    p = orc.prepare(qb, kb, vb, flags=flags, signs=synth.hadamard_signs(9, d))
+    table = orc.e4m3_decode_table()
+
+    def deq_tiles(codes, ds, H_):
+        ds = np.repeat(ds.reshape(B, H_, nt), TS, axis=2)[:, :, :N].astype(np.float64)
+        return table[codes] * ds[..., None]
+
+    qd = deq_tiles(p["q8"], p["q_descale"], Hq)
+    kd = deq_tiles(p["k8"], p["k_descale"], Hkv)
+    vd = table[p["v8"]] * p["v_descale"].reshape(B, Hkv, 1, 1).astype(np.float64)
+    scale = 1.0 / math.sqrt(d) / (d if rotate else 1)
+    ref = _sdpa(qd, kd, vd, True, scale=scale).reshape(B * Hq, N, d)
+    for T in (64, 128):
+        O, _ = orc.attn_quant(p, (B, Hq, Hkv, N, d), flags, 1.0, 1, True, T, mode=orc.NO_PCAST)
+        rel = np.linalg.norm(O - ref, axis=(1, 2)) / np.linalg.norm(ref, axis=(1, 2))
+        assert rel.max() < 1e-5

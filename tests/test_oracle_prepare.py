@@ -122,3 +122,54 @@ def test_prepare_zero_slice_gives_unit_scale(orc):
     v[:] = 0
     p = orc.prepare(q, k, v)
     assert p["v_descale"][0] == 1.0 and np.all(p["v8"] == 0)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_prepare_tile_scales(orc, flags):
+    """Per-tile scales: every 128-row tile of Q and K has descale = its own amax / 448
+    (amax from an independent float64 transform), reaches the saturation code, and
+    reconstructs within the E4M3 bound of its own scale; V keeps one scale per slice."""
+    B, Hq, Hkv, N, d, TS = 1, 2, 2, 300, 64, 128
+    nt = (N + TS - 1) // TS
+    qb, kb, vb = synth.qwen_like_inputs(61 + flags, B, Hq, Hkv, N, d, key_norm=30.0, key_channels=4)
+    signs = synth.hadamard_signs(78, d)
+    p = orc.prepare(qb, kb, vb, flags=flags | orc.TILE_SCALES, signs=signs)
+    slice_p = orc.prepare(qb, kb, vb, flags=flags, signs=signs)
+    assert p["q_descale"].shape == (B * Hq * nt,) and p["k_descale"].shape == (B * Hkv * nt,)
+    assert np.array_equal(p["v8"], slice_p["v8"]) and np.array_equal(p["v_descale"], slice_p["v_descale"])
+    table = orc.e4m3_decode_table()
+    q = synth.bf16_bits_to_f32(qb).astype(np.float64)
+    k = synth.bf16_bits_to_f32(kb).astype(np.float64)
+    H = scipy.linalg.hadamard(d).astype(np.float64)
+    if flags & 2:
+        k = k - p["k_mean"].reshape(B, Hkv, 1, d).astype(np.float64)
+    if flags & 1:
+        q = (q * signs) @ H
+        k = (k * signs) @ H
+    for name, x, ds, H_ in (("q8", q, p["q_descale"], Hq), ("k8", k, p["k_descale"], Hkv)):
+        ds = ds.reshape(B, H_, nt)
+        codes = p[name]
+        for t in range(nt):
+            xt = x[:, :, t * TS:(t + 1) * TS]
+            ct = codes[:, :, t * TS:(t + 1) * TS]
+            amax = np.abs(xt).reshape(B, H_, -1).max(-1)
+            np.testing.assert_allclose(ds[:, :, t], amax / 448.0, rtol=1e-5)
+            assert np.all((np.abs(table[ct]).reshape(B, H_, -1) == 448.0).any(-1))
+            deq = table[ct].astype(np.float64) * ds[:, :, t].reshape(B, H_, 1, 1).astype(np.float64)
+            bound = np.maximum(np.abs(xt) * 2.0 ** -4, 2.0 ** -10 * ds[:, :, t].reshape(B, H_, 1, 1)) + 1e-6 * np.abs(xt)
+            assert np.all(np.abs(deq - xt) <= bound), (name, t)
+
+
+def test_tile_scales_reduce_to_slice_scales_when_tiles_share_amax(orc):
+    """If every tile holds the slice's largest magnitude, the per-tile scales all equal
+    the slice scale and the codes are those of the full-sequence scaling."""
+    B, Hq, Hkv, N, d = 1, 2, 1, 384, 64
+    q, k, v = synth.qkv_normal(62, B, Hq, Hkv, N, d)
+    for x in (q, k):
+        x /= np.abs(x).max() * 1.01  # |x| < 1
+        x[:, :, ::128, 0] = 3.0     # one entry of 3 in every 128-row tile
+    p = orc.prepare(q, k, v, flags=orc.TILE_SCALES)
+    s = orc.prepare(q, k, v, flags=0)
+    assert np.array_equal(p["q8"], s["q8"]) and np.array_equal(p["k8"], s["k8"])
+    assert np.all(p["q_descale"].reshape(B * Hq, -1) == s["q_descale"][:, None])
+    assert np.all(p["k_descale"].reshape(B * Hkv, -1) == s["k_descale"][:, None])
