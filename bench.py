@@ -337,6 +337,8 @@ def run_ours(args):
     B, Hq, Hkv, N, d, T = WL["B"], WL["Hq"], WL["Hkv"], WL["N"], WL["d"], WL["kv_tile"]
     S = WL["S"]
     flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT
+    if args.scales == "tile":
+        flags |= aq.ATTNQ_TILE_SCALES
     q_np, k_np, v_np = make_inputs(replica_seed(rank))
     signs_np = synth.hadamard_signs(17, d)
     dev = torch.device("cuda", local)
@@ -454,7 +456,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "rotate": True, "center_k": True, "in_dtype": "bf16",
+            "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "rotate": True, "center_k": True, "scales": "per-tile (128 tokens)" if args.scales == "tile" else "per (batch, head)", "in_dtype": "bf16",
                        "out_dtype": "bf16", "step": "attnq_prepare + attnq_fwd",
                        "l2": "inputs 805 MB per step > 129 MB L2; no flush",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -495,6 +497,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=96)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--scales", choices=["slice", "tile"], default="slice",
+                    help="Q/K scales per (batch, head) (the timed workload) or per 128-token tile")
     ap.add_argument("--B", type=int, default=WL["B"], help="smaller batch for profiling captures")
     ap.add_argument("--Hq", type=int, default=WL["Hq"])
     ap.add_argument("--Hkv", type=int, default=WL["Hkv"])

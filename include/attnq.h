@@ -52,7 +52,9 @@ typedef enum {
 } attnq_status;
 
 /* desc.flags */
-enum { ATTNQ_ROTATE = 1u, ATTNQ_CENTER_K = 2u, ATTNQ_VT_LAYOUT = 4u };
+enum { ATTNQ_ROTATE = 1u, ATTNQ_CENTER_K = 2u, ATTNQ_VT_LAYOUT = 4u, ATTNQ_TILE_SCALES = 8u };
+/* tokens per scale tile of ATTNQ_TILE_SCALES */
+enum { ATTNQ_SCALE_TILE = 128 };
 /* element types of Q/K/V inputs and of O */
 enum { ATTNQ_F32 = 0, ATTNQ_BF16 = 1 };
 /* KV-tile visiting order of the online softmax [PC sec. 1] */
@@ -68,7 +70,13 @@ enum { ATTNQ_KV_FORWARD = 0, ATTNQ_KV_REVERSE = 1 };
  *   ATTNQ_CENTER_K  subtract from K the mean key of its (batch, KV head) over
  *                   all N tokens, before rotation [AN], [RR];
  *   ATTNQ_VT_LAYOUT v8 is stored transposed, [B, Hkv, d, ldv] with
- *                   ldv = attnq_vt_ld(N) (tokens N .. ldv-1 are zero).
+ *                   ldv = attnq_vt_ld(N) (tokens N .. ldv-1 are zero);
+ *   ATTNQ_TILE_SCALES  Q and K get one max-based scale per 128-token tile of
+ *                   each (batch, head), tiles aligned at token 0, instead of
+ *                   one per (batch, head) (the emulator's per-tile scales that
+ *                   the "attention-numerics" page, method and kernel settings,
+ *                   contrasts with the API's full-sequence scales); V keeps
+ *                   one scale per (batch, head).
  * signs: DEVICE pointer to d int8 values, each +1 or -1; required when
  * ATTNQ_ROTATE is set, ignored otherwise.
  */
@@ -82,6 +90,8 @@ typedef struct {
 /*
  * Per-(batch, head) descales (amax / 448, fp32) written by attnq_prepare and
  * read by attnq_fwd: q_descale [B*Hq], k_descale and v_descale [B*Hkv].
+ * With ATTNQ_TILE_SCALES: q_descale [B*Hq*nt] and k_descale [B*Hkv*nt],
+ * nt = attnq_scale_tiles(N), tile t of slice s at s*nt + t; v_descale as above.
  * k_mean: optional [B*Hkv*d] fp32 output of the mean key (may be NULL).
  */
 typedef struct {
@@ -90,6 +100,9 @@ typedef struct {
   float* v_descale;
   float* k_mean;
 } attnq_scales;
+
+/* Scale tiles per (batch, head) slice: ceil(N / ATTNQ_SCALE_TILE); 0 if N <= 0. */
+int32_t attnq_scale_tiles(int32_t N);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t attnq_version(void);
@@ -164,12 +177,15 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
  * (every key when causal == 0), visited forward (0 -> diagonal) or reverse
  * (diagonal -> 0):
  *   s_j = q8_i . k8_j (exact products, fp32 accumulation);
- *   t_j = s_j * c,  c = fl32(dq * dk / sqrt(d) * (ROTATE ? 1/d : 1) * log2 e);
+ *   t_j = s_j * c,  c = fl32(cq * dk), cq = fl32(dq / sqrt(d) * (ROTATE ? 1/d : 1) * log2 e)
+ *   (cq in double);
  *   m' = max(m, max_j t_j);  alpha = 2^(m - m');  P_j = 2^(t_j - m');
  *   l = alpha * l + sum_j P_j;  p8_j = E4M3(P_j * S);
  *   acc = alpha * acc + sum_j p8_j * v8_j;
  * and finally O = acc * dv / (S * l).  The running maximum is exact (no
- * lazy rescaling).  desc: shape and flags of the attnq_prepare call that made
+ * lazy rescaling).  With ATTNQ_TILE_SCALES, dq is row i's query tile's and dk
+ * key j's tile's descale (kv_tile divides the scale tile, so c is constant
+ * within a KV tile).  desc: shape and flags of the attnq_prepare call that made
  * the operands (ATTNQ_VT_LAYOUT is required; in_dtype is ignored).
  * q8, k8, v8, scales: DEVICE, as written by attnq_prepare.  S: finite, in
  * (0, 448].  kv_order: ATTNQ_KV_FORWARD or ATTNQ_KV_REVERSE.  kv_tile: 64 or

@@ -470,12 +470,14 @@ void emulate_row(const RowCtx& x, int i, const double* qrow, KeyF key, ValF val,
 extern "C" {
 
 // Quantised forward on E4M3 operands in the natural [B, H, N, d] layout.
-// c = fl32(dq * dk * (1/sqrt d) * (ROTATE ? 1/d : 1) * log2 e), evaluated in
-// double: the unnormalised FWHT on Q and K multiplies q.k by exactly d.
-// Softmax scale reading: the pages do not state it; the standard 1/sqrt(d).
-// With ORC_TILE_SCALES, q_ds and k_ds hold one descale per scale tile and c is
-// formed, in the same order, from the query row's tile and the key's tile
-// (the key tiles T divide the scale tile, so c is constant within a key tile).
+// c = fl32(cq * dk) with cq = fl32(dq * (1/sqrt d) * (ROTATE ? 1/d : 1) * log2 e)
+// evaluated in double: the unnormalised FWHT on Q and K multiplies q.k by
+// exactly d.  Softmax scale reading: the pages do not state it; the standard
+// 1/sqrt(d).  The pages fix no evaluation order for c; this one needs a
+// single fp32 multiply per key scale.  With ORC_TILE_SCALES, q_ds and k_ds hold
+// one descale per scale tile, cq is the query row's tile's and dk the key's
+// tile's (the key tiles T divide the scale tile, so c is constant within a
+// key tile).
 int orc_attn_quant(int B, int Hq, int Hkv, int N, int d, unsigned flags, const uint8_t* q8, const uint8_t* k8,
                    const uint8_t* v8, const float* q_ds, const float* k_ds, const float* v_ds, float S, int kv_order,
                    int causal, int T, int k_sink, int mode, const int32_t* bh_list, int n_bh, const int32_t* rows,
@@ -500,8 +502,8 @@ int orc_attn_quant(int B, int Hq, int Hkv, int N, int d, unsigned flags, const u
     const uint8_t* kh = k8 + (int64_t(b) * Hkv + g) * slice;
     const uint8_t* vh = v8 + (int64_t(b) * Hkv + g) * slice;
     auto logit_factor = [&](float dq, float dk) {
-      return float(double(dq) * double(dk) * (1.0 / std::sqrt(double(d))) * (rotate ? 1.0 / double(d) : 1.0) *
-                   LOG2E);
+      const float cq = float(double(dq) * (1.0 / std::sqrt(double(d))) * (rotate ? 1.0 / double(d) : 1.0) * LOG2E);
+      return cq * dk;
     };
     const float* qd = q_ds + (int64_t(b) * Hq + h) * nst;
     const float* kd = k_ds + (int64_t(b) * Hkv + g) * nst;

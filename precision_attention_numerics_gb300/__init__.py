@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     ATTNQ_KV_FORWARD,
     ATTNQ_KV_REVERSE,
     ATTNQ_ROTATE,
+    ATTNQ_SCALE_TILE,
+    ATTNQ_TILE_SCALES,
     ATTNQ_VT_LAYOUT,
     AttnqDesc,
     AttnqError,
@@ -34,6 +36,7 @@ from .binding import (  # noqa: F401
     ATTNQ_STATIC_SCRATCH_BYTES,
     attnq_prepare_workspace,
     attnq_ref_attention,
+    attnq_scale_tiles,
     attnq_set_wait_limit_ns,
     attnq_status_string,
     attnq_version,

@@ -16,6 +16,8 @@ import numpy as np
 ATTNQ_ROTATE = 1
 ATTNQ_CENTER_K = 2
 ATTNQ_VT_LAYOUT = 4
+ATTNQ_TILE_SCALES = 8
+ATTNQ_SCALE_TILE = 128
 ATTNQ_F32 = 0
 ATTNQ_BF16 = 1
 ATTNQ_KV_FORWARD = 0
@@ -94,6 +96,8 @@ def load_library():
     L.attnq_status_string.argtypes = [i32]
     L.attnq_vt_ld.restype = i64
     L.attnq_vt_ld.argtypes = [i32]
+    L.attnq_scale_tiles.restype = i32
+    L.attnq_scale_tiles.argtypes = [i32]
     L.attnq_hadamard_signs.restype = i32
     L.attnq_hadamard_signs.argtypes = [C.c_uint64, i32, P]
     L.attnq_prepare_workspace.restype = sz
@@ -160,6 +164,10 @@ def attnq_status_string(code: int) -> str:
 
 def attnq_vt_ld(N: int) -> int:
     return int(load_library().attnq_vt_ld(N))
+
+
+def attnq_scale_tiles(N: int) -> int:
+    return int(load_library().attnq_scale_tiles(N))
 
 
 def attnq_hadamard_signs(seed: int, d: int) -> np.ndarray:

@@ -3,7 +3,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-from .binding import ATTNQ_VT_LAYOUT, AttnqDesc, AttnqScales, attnq_prepare_workspace, attnq_vt_ld
+from .binding import (ATTNQ_TILE_SCALES, ATTNQ_VT_LAYOUT, AttnqDesc, AttnqScales, attnq_prepare_workspace,
+                      attnq_scale_tiles, attnq_vt_ld)
 
 
 @dataclass
@@ -25,8 +26,9 @@ def alloc_prepared(desc: AttnqDesc, device="cuda", with_mean: bool = True) -> Pr
         v8 = torch.empty((B, Hkv, d, attnq_vt_ld(N)), dtype=torch.uint8, device=device)
     else:
         v8 = torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=device)
-    scales = AttnqScales(torch.empty(B * Hq, dtype=torch.float32, device=device),
-                         torch.empty(B * Hkv, dtype=torch.float32, device=device),
+    nst = attnq_scale_tiles(N) if desc.flags & ATTNQ_TILE_SCALES else 1  # descales per Q/K slice
+    scales = AttnqScales(torch.empty(B * Hq * nst, dtype=torch.float32, device=device),
+                         torch.empty(B * Hkv * nst, dtype=torch.float32, device=device),
                          torch.empty(B * Hkv, dtype=torch.float32, device=device),
                          torch.empty(B * Hkv * d, dtype=torch.float32, device=device) if with_mean else None)
     ws = torch.empty(max(attnq_prepare_workspace(desc), 256), dtype=torch.uint8, device=device)

@@ -57,7 +57,8 @@ attnq_status check_desc(const attnq_desc* d) {
   if (!d) return ATTNQ_EINVAL;
   if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0 || d->d <= 0) return ATTNQ_EINVAL;
   if (d->Hq % d->Hkv != 0) return ATTNQ_EINVAL;
-  if ((d->flags & ~uint32_t(ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT)) != 0) return ATTNQ_EINVAL;
+  if ((d->flags & ~uint32_t(ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT | ATTNQ_TILE_SCALES)) != 0)
+    return ATTNQ_EINVAL;
   if (d->d != 64 && d->d != 128) return ATTNQ_EUNSUPPORTED;
   // grid.y of the prepare passes and int32 indices of rows
   const int64_t nslices = int64_t(d->B) * d->Hq + 2 * int64_t(d->B) * d->Hkv;
@@ -132,11 +133,12 @@ PipeLayout pipe_layout(const attnq_desc* d, int32_t out_dtype) {
   L.in_bytes[2] = es * nk * rows;
   for (int b = 0; b < 2; ++b)
     for (int t = 0; t < 3; ++t) L.in[b][t] = take(L.in_bytes[t]);
+  const size_t nst = (d->flags & ATTNQ_TILE_SCALES) ? size_t(attnq_scale_tiles(d->N)) : 1;
   L.q8 = take(nq * rows);
   L.k8 = take(nk * rows);
   L.v8 = take(nk * size_t(d->d) * size_t(attnq_vt_ld(d->N)));
-  L.q_ds = take(4 * nq);
-  L.k_ds = take(4 * nk);
+  L.q_ds = take(4 * nq * nst);
+  L.k_ds = take(4 * nk * nst);
   L.v_ds = take(4 * nk);
   L.k_mean = take(4 * nk * d->d);
   L.prep = take(attnq_prepare_workspace(d));
@@ -220,6 +222,8 @@ const char* attnq_status_string(attnq_status s) {
   return "unknown attnq status";
 }
 
+int32_t attnq_scale_tiles(int32_t N) { return N <= 0 ? 0 : (N + ATTNQ_SCALE_TILE - 1) / ATTNQ_SCALE_TILE; }
+
 int64_t attnq_vt_ld(int32_t N) { return N <= 0 ? 0 : (int64_t(N) + 15) / 16 * 16; }
 
 attnq_status attnq_hadamard_signs(uint64_t seed, int32_t d, int8_t* host_out) {
@@ -262,6 +266,7 @@ attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K,
   a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
   a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
   a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
+  a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
   a.signs = desc->signs;
   a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
   a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
@@ -298,6 +303,7 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
   a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
   a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
   a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
+  a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
   a.signs = desc->signs;
   a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
   a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
@@ -332,6 +338,7 @@ attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t*
   a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d; a.T = kv_tile;
   a.causal = causal; a.reverse = kv_order == ATTNQ_KV_REVERSE;
   a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
+  a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
   a.S = S;
   a.q8 = q8; a.k8 = k8; a.v8t = v8; a.ldv = attnq_vt_ld(desc->N);
   a.q_ds = scales->q_descale; a.k_ds = scales->k_descale; a.v_ds = scales->v_descale;

@@ -67,6 +67,7 @@ namespace attnq {
 namespace {
 
 constexpr int kRows = 128;
+static_assert(kRows == kScaleTile, "a query tile is one scale tile");
 constexpr int kThreads = 384;          // three warpgroups
 constexpr int kProducerWarp = 8, kMmaWarp = 9;  // warps 9 and 10 issue the MMAs of warpgroups 0 and 1
 // Register split: launched at 168 per thread (384 x 168 = 64,512); the two
@@ -85,6 +86,8 @@ struct Params {
   const float* q_ds;
   const float* k_ds;
   const float* v_ds;
+  int tiles;   // 1: q_ds and k_ds hold one descale per 128-token tile (n_st per slice)
+  int n_st;    // scale tiles per slice
   double inv_sqrt_d, rot, log2e;
   void* O;
   int out_bf16;
@@ -378,7 +381,7 @@ __device__ __forceinline__ uint32_t p_tile_offset(int r, int c) {
   }
 }
 
-template <int D, int T, bool COUNT>
+template <int D, int T, bool COUNT, bool TILES>
 __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem, uint8_t* sP, const Bars& br,
                                            volatile int* abort_flag) {
   const int r = threadIdx.x & 127;           // row in the query tile = TMEM lane
@@ -398,10 +401,20 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
     if (w >= un.nact) continue;  // sits the unit out: no arrival on o_free (its warps would not be in step)
     const int h = un.h0 + w;
     const int bh = un.b * p.Hq + h, bg = un.b * p.Hkv + un.g;
-    const float c = __double2float_rn(
-        __dmul_rn(__dmul_rn(__dmul_rn(__dmul_rn(double(p.q_ds[bh]), double(p.k_ds[bg])), p.inv_sqrt_d), p.rot),
-                  p.log2e));
-    const uint64_t c2 = pack2(c, c);
+    // logit factor c = fl32(cq * dk), cq = fl32(dq * (1/sqrt d) * rot * log2 e)
+    // in double once per unit; with per-tile scales dq is the query tile's and
+    // dk the key tile's (one fp32 multiply per key tile, its descale loaded a
+    // tile ahead)
+    const double dq = double(TILES ? p.q_ds[int64_t(bh) * p.n_st + un.t] : p.q_ds[bh]);
+    const float cq = __double2float_rn(__dmul_rn(__dmul_rn(__dmul_rn(dq, p.inv_sqrt_d), p.rot), p.log2e));
+    const float* kd = TILES ? p.k_ds + int64_t(bg) * p.n_st : p.k_ds + bg;
+    auto key_scale_tile = [&](int k) { return ((p.reverse ? un.nt - 1 - k : k) * T) / kScaleTile; };
+    float c = __fmul_rn(cq, kd[TILES ? key_scale_tile(0) : 0]);
+    float dk_next = 0.0f;
+    if constexpr (TILES) {
+      if (un.nt > 1) dk_next = kd[key_scale_tile(1)];
+    }
+    uint64_t c2 = pack2(c, c);
     const int i = un.t * kRows + r;
     float m = -INFINITY, l = 0.0f;
     uint32_t uf0 = 0, uf1 = 0;
@@ -411,6 +424,13 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       if (!warp_wait(br.s_full + w, sc & 1u, p, abort_flag)) { ok = false; break; }
       ++sc;
       tc_fence_after();
+      if constexpr (TILES) {
+        if (k > 0) {
+          c = __fmul_rn(cq, dk_next);
+          c2 = pack2(c, c);
+          if (k + 1 < un.nt) dk_next = kd[key_scale_tile(k + 1)];
+        }
+      }
       const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
       // keys j0 + j are visible for j < lim (causal: j0 + j <= i; always j0 + j < N)
       const int lim = need_mask ? min(p.N - j0, p.causal ? i - j0 + 1 : T) : T;
@@ -493,7 +513,11 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
               for (int e = 0; e < 4; ++e) {
                 const int jj = j0 + 4 * q + e;
                 const uint32_t code = (pw[qq] >> (8 * e)) & 0xFFu;
-                if (PS[e] > 0.0f && code == 0u && jj >= p.k_sink) {
+                // P itself, 2^(fl(fl(s c) - m')) in fp32, is 0 once its exponent is
+                // at most -150 (2^-150 rounds to 0); P*S formed in one step can
+                // still be positive there, but P*S of a zero P is no underflow
+                const bool p_pos = __fsub_rn(__fmul_rn(sv[4 * q + e], c), muse) > -150.0f;
+                if (PS[e] > 0.0f && p_pos && code == 0u && jj >= p.k_sink) {
                   if (jt == 0) ++uf0;
                   else ++uf1;
                 }
@@ -593,7 +617,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
   if (!ok) raise_abort(p, abort_flag);
 }
 
-template <int D, int T, bool COUNT>
+template <int D, int T, bool COUNT, bool TILES>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const Params p) {
@@ -669,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     regs_increase<kSoftmaxRegs>();
-    softmax_wg<D, T, COUNT>(p, warp >> 2, tmem, sP, br, abort_flag);
+    softmax_wg<D, T, COUNT, TILES>(p, warp >> 2, tmem, sP, br, abort_flag);
   }
 
   tc_fence_before();
@@ -680,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int T, bool COUNT>
+template <int D, int T, bool COUNT, bool TILES>
 cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   using C = Cfg<D, T>;
   CUtensorMap tq, tk, tv;
@@ -709,6 +733,8 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   p.q_ds = a.q_ds;
   p.k_ds = a.k_ds;
   p.v_ds = a.v_ds;
+  p.tiles = a.tiles;
+  p.n_st = (a.N + kScaleTile - 1) / kScaleTile;
   p.inv_sqrt_d = 1.0 / std::sqrt(double(D));
   p.rot = a.rotate ? 1.0 / double(D) : 1.0;
   p.log2e = 1.4426950408889634073599246810018921;
@@ -718,7 +744,7 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   p.k_sink = a.k_sink;
   p.status = a.status;
   p.wait_ns = a.wait_ns;
-  auto kern = k_attn_fwd<D, T, COUNT>;
+  auto kern = k_attn_fwd<D, T, COUNT, TILES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
@@ -728,7 +754,8 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
 
 template <int D, int T>
 cudaError_t run_count(const FwdArgs& a, cudaStream_t st) {
-  return a.underflow ? run<D, T, true>(a, st) : run<D, T, false>(a, st);
+  if (a.tiles) return a.underflow ? run<D, T, true, true>(a, st) : run<D, T, false, true>(a, st);
+  return a.underflow ? run<D, T, true, false>(a, st) : run<D, T, false, false>(a, st);
 }
 
 }  // namespace

@@ -9,10 +9,14 @@
 namespace attnq {
 
 // ---- prepare -------------------------------------------------------------
+// Tokens per scale tile of the per-tile Q/K scales (tiles aligned at token 0).
+constexpr int kScaleTile = 128;
+
 struct PrepareArgs {
   int B, Hq, Hkv, N, d;
   int bf16;           // input element type: 1 bf16, 0 fp32
   int rotate, center, vt;
+  int tiles;          // per-tile Q/K scales
   const int8_t* signs;
   const void* Q;
   const void* K;
@@ -52,6 +56,7 @@ struct FwdArgs {
   int B, Hq, Hkv, N, d, T;
   int causal, reverse;
   int rotate;
+  int tiles;          // per-tile Q/K scales
   float S;
   const uint8_t* q8;
   const uint8_t* k8;

@@ -57,6 +57,7 @@ constexpr int kFlowThreads = 384;  // two consumer warpgroups + a warpgroup whos
 // 2 x 128 x 232 + 128 x 40 = 64,512.
 constexpr uint32_t kConsumerRegs = 232, kProducerRegs = 40;
 static_assert(2 * 128 * kConsumerRegs + 128 * kProducerRegs <= kFlowThreads * 168, "register split");
+static_assert(kTR == kScaleTile, "a ring tile is one scale tile");
 constexpr int kLagA = 4, kLagC = 7;  // least list steps from a K slice's M entry to its A entry; A to C
 constexpr uint32_t KIND_M = 0u, KIND_A = 1u, KIND_C = 2u, KIND_DONE = 3u;
 constexpr uint32_t CTL_TICKET = 0, CTL_ABORT = 1, CTL_ENTRIES = 2;
@@ -77,7 +78,8 @@ struct FlowCfg {
   static constexpr int NST = NST1 - NST1 % kGroups;
   static constexpr int WORDS = BF16 ? D / 2 : D;  // 32-bit input words per row
   static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(2 * kConsumerWarps) * WB + 16 * NST +
-                                 16 * NST + 4 * WORDS + 8 * (D / 2) + kConsumerWarps * 8 * (D / 2);
+                                 16 * NST + 4 * WORDS + 8 * (D / 2) + kConsumerWarps * 8 * (D / 2) +
+                                 4 * 4 * 2 * kGroups + 8 * 2 * kGroups;
   static_assert(NST >= kGroups && NST % kGroups == 0, "pipeline depth: whole stages per group");
   static_assert(SMEM <= 232448, "shared memory budget");
 };
@@ -140,20 +142,53 @@ __global__ void k_flow_init(PrepareArgs a) {
     if (i < L) return k0 + (nk - L) + i;
     return i - L;
   };
-  // Step t holds, in this order: C of the slice whose A entry was kLagC steps
-  // earlier, A, M.  Entries before step t: the C, A and M entries of steps
-  // 0 .. t-1, so every thread writes its steps' entries in place.
-  const int nsteps = ns + kLagC;
+  // A list step holds up to five entries, in a fixed order of kinds; each kind
+  // occupies an interval [lo, hi) of steps, so the entries before step t are
+  // counted in closed form and every thread writes its steps' entries in place.
+  //   full-sequence scales: C of the slice whose A entry was kLagC steps
+  //     earlier, A (aorder), M of K slice t;
+  //   per-tile scales (Q and K need no A pass): C of V slice t - kLagC, C of K
+  //     slice t - Lk (Lk = kLagA with centring, after its M entry), A of V
+  //     slice t, M of K slice t, C of Q slice t.
+  const int Lk = a.center ? kLagA : 0;
+  int lo[5], hi[5];
+  uint32_t kinds[5];
+  int nk_kinds;
+  if (!a.tiles) {
+    nk_kinds = 3;
+    lo[0] = kLagC; hi[0] = ns + kLagC; kinds[0] = KIND_C;
+    lo[1] = 0; hi[1] = ns; kinds[1] = KIND_A;
+    lo[2] = 0; hi[2] = a.center ? nk : 0; kinds[2] = KIND_M;
+  } else {
+    nk_kinds = 5;
+    lo[0] = kLagC; hi[0] = nk + kLagC; kinds[0] = KIND_C;
+    lo[1] = Lk; hi[1] = nk + Lk; kinds[1] = KIND_C;
+    lo[2] = 0; hi[2] = nk; kinds[2] = KIND_A;
+    lo[3] = 0; hi[3] = a.center ? nk : 0; kinds[3] = KIND_M;
+    lo[4] = 0; hi[4] = nq; kinds[4] = KIND_C;
+  }
+  auto slice_of = [&](int kind_idx, int t) -> int {
+    if (!a.tiles) return kind_idx == 0 ? aorder(t - kLagC) : kind_idx == 1 ? aorder(t) : k0 + t;
+    switch (kind_idx) {
+      case 0: return v0 + (t - kLagC);
+      case 1: return k0 + (t - Lk);
+      case 2: return v0 + t;
+      case 3: return k0 + t;
+      default: return t;
+    }
+  };
+  int nsteps = 0;
+  for (int x = 0; x < nk_kinds; ++x) nsteps = max(nsteps, hi[x]);
   auto first = [&](int t) -> uint32_t {
-    const int c = (t < nsteps ? t : nsteps) - kLagC;
-    return uint32_t((c > 0 ? c : 0) + (t < ns ? t : ns) + (a.center ? (t < nk ? t : nk) : 0));
+    uint32_t e = 0;
+    for (int x = 0; x < nk_kinds; ++x)
+      if (hi[x] > lo[x]) e += uint32_t(min(max(t, lo[x]), hi[x]) - lo[x]);
+    return e;
   };
   for (int t = threadIdx.x; t < nsteps; t += blockDim.x) {
     uint32_t e = first(t);
-    const int tc = t - kLagC;
-    if (tc >= 0 && tc < ns) a.entries[e++] = (KIND_C << 30) | uint32_t(aorder(tc));
-    if (t < ns) a.entries[e++] = (KIND_A << 30) | uint32_t(aorder(t));
-    if (a.center && t < nk) a.entries[e++] = (KIND_M << 30) | uint32_t(k0 + t);
+    for (int x = 0; x < nk_kinds; ++x)
+      if (t >= lo[x] && t < hi[x]) a.entries[e++] = (kinds[x] << 30) | uint32_t(slice_of(x, t));
   }
   if (threadIdx.x == 0) {
     a.ctl[CTL_TICKET] = 0u;
@@ -556,6 +591,10 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   uint32_t* smask = reinterpret_cast<uint32_t*>(empty + C::NST);  // sign-bit mask per input word
   uint64_t* pmask = reinterpret_cast<uint64_t*>(smask + C::WORDS);  // sign-bit masks of the pairs (x_j, x_{j+D/2})
   uint64_t* nmu_all = pmask + D / 2;                               // per consumer warp: -mu as pairs [D/2]
+  // per-tile scales: each group's four warp maxima of a tile, two slots by
+  // tile parity, and the barriers (four arrivals) that publish them
+  uint32_t* tmax = reinterpret_cast<uint32_t*>(nmu_all + kConsumerWarps * (D / 2));  // [group][2][4]
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(tmax + 4 * 2 * kGroups);              // [group][2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -563,6 +602,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       mbar_init(full + s, 1);
       mbar_init(empty + s, 4);  // one arrival per consumer warp of the stage's group
     }
+    for (int x = 0; x < 2 * kGroups; ++x) mbar_init(xbar + x, 4);
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < C::WORDS; i += blockDim.x) {
@@ -613,6 +653,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   bool ok = true;
   uint32_t run_max = 0;    // amax bits of this lane's rows in the current item
   uint32_t run_tiles = 0;  // tiles of the current item this warp has finished
+  uint32_t xc = 0;         // per-tile scale exchanges of this warp's group
   for (uint32_t j = 0;; ++j) {
     const uint32_t n = 2u * j + uint32_t(g);
     const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
@@ -703,21 +744,44 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       continue;
     }
 
-    // KIND_C: the slice's scale, the last stage, codes, staged for a TMA store
-    if (qs_slice != s) {
-      // every A tile of the slice has added its amax (acquire on the count)
-      if (!warp_count_wait(a, a.a_done + s, tiles * 4u)) { ok = false; break; }
-      qs_bits = __ldcg(a.amax_bits + s);
+    // KIND_C: the scale (the slice's, or with per-tile scales the tile's), the
+    // last stage, codes staged for a TMA store
+    if (a.tiles && qk) {
+      // the tile's amax from its four warps, exchanged through shared memory
+      uint32_t mx = valid ? (rotate ? rotated_amax_bits<D>(P) : plain_amax_bits<D>(P)) : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const uint32_t xb = 2u * uint32_t(g) + (xc & 1u);
+      if (lane == 0) {
+        tmax[4 * xb + w4] = mx;
+        mbar_arrive(xbar + xb);
+      }
+      if (!warp_bar_wait(a, xbar + xb, (xc >> 1) & 1u)) { ok = false; break; }
+      ++xc;
+      const uint32_t bits = max(max(tmax[4 * xb], tmax[4 * xb + 1]), max(tmax[4 * xb + 2], tmax[4 * xb + 3]));
       float ds;
-      scale_from_amax(qs_bits, qs, ds);
-      qs_slice = s;
-    }
-    if (row0 == 0 && w4 == 0 && lane == 0) {
-      // the warp with the slice's first rows publishes its descale
-      float q2, ds;
-      scale_from_amax(qs_bits, q2, ds);
-      (sr.tensor == 0 ? a.q_ds : sr.tensor == 1 ? a.k_ds : a.v_ds)[sr.local] = ds;
-      if (qs_bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
+      scale_from_amax(bits, qs, ds);
+      qs_slice = -1;  // qs is this tile's
+      if (w4 == 0 && lane == 0) {
+        (sr.tensor == 0 ? a.q_ds : a.k_ds)[int64_t(sr.local) * tiles + uint32_t(row0 / kScaleTile)] = ds;
+        if (bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
+      }
+    } else {
+      if (qs_slice != s) {
+        // every A tile of the slice has added its amax (acquire on the count)
+        if (!warp_count_wait(a, a.a_done + s, tiles * 4u)) { ok = false; break; }
+        qs_bits = __ldcg(a.amax_bits + s);
+        float ds;
+        scale_from_amax(qs_bits, qs, ds);
+        qs_slice = s;
+      }
+      if (row0 == 0 && w4 == 0 && lane == 0) {
+        // the warp with the slice's first rows publishes its descale
+        float q2, ds;
+        scale_from_amax(qs_bits, q2, ds);
+        (sr.tensor == 0 ? a.q_ds : sr.tensor == 1 ? a.k_ds : a.v_ds)[sr.local] = ds;
+        if (qs_bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
+      }
     }
     if (rotate) final_stage<D>(P);
     uint32_t cw[D / 4];

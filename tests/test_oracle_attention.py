@@ -106,7 +106,8 @@ def _closed_form_rows(table, q8, k8, v8, qd, kd, vd, d, rotate, S, order, T, k_s
     """Online softmax with the running-max rescales multiplied out:
     O = sum_j dec(p8_j) v_j 2^(m_tile(j) - m_final) * dv / (S * sum_j P_j 2^(m_tile(j) - m_final))."""
     N = q8.shape[0]
-    c = np.float32(float(qd) * float(kd) / math.sqrt(d) * (1.0 / d if rotate else 1.0) / math.log(2.0))
+    cq = np.float32(float(qd) / math.sqrt(d) * (1.0 / d if rotate else 1.0) / math.log(2.0))
+    c = np.float32(cq * np.float32(kd))
     qf, kf, vf = table[q8], table[k8], table[v8]
     out = np.zeros((N, d))
     uf = np.zeros(2, np.int64)
