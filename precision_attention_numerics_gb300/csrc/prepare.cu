@@ -50,13 +50,14 @@ constexpr int kTR = 128;           // rows per tile = tokens per mean-key chunk
 constexpr int kTilesPerItem = 16;  // tiles per claimed item
 constexpr int kGroups = 2;         // consumer groups (4 warps, one row per thread)
 constexpr int kConsumerWarps = 4 * kGroups;
-constexpr int kFlowThreads = 384;  // two consumer warpgroups + a warpgroup whose warp 8 is the producer
-// Register split: launched at 168 per thread (384 x 168 = 64,512); the consumer
-// warpgroups rise to 232 (a row of 128 fp32 values and the FWHT's working set
-// fit without spilling), the producer's warpgroup drops to 40:
-// 2 x 128 x 232 + 128 x 40 = 64,512.
-constexpr uint32_t kConsumerRegs = 232, kProducerRegs = 40;
-static_assert(2 * 128 * kConsumerRegs + 128 * kProducerRegs <= kFlowThreads * 168, "register split");
+constexpr int kFlowThreads = 128 * (kGroups + 1);  // consumer warpgroups + a warpgroup whose first warp is the producer
+// Register split: launched at the even share of the register file (168 per
+// thread for 384 threads); the consumer warpgroups rise to hold a row of 128
+// fp32 values and the FWHT's working set without spilling, the producer's
+// warpgroup drops: 2 x 128 x 232 + 128 x 40 = 64,512.
+constexpr uint32_t kLaunchRegs = (65536u / kFlowThreads) & ~7u;
+constexpr uint32_t kConsumerRegs = kGroups == 2 ? 232 : 160, kProducerRegs = kGroups == 2 ? 40 : 32;
+static_assert(kGroups * 128 * kConsumerRegs + 128 * kProducerRegs <= kFlowThreads * kLaunchRegs, "register split");
 static_assert(kTR == kScaleTile, "a ring tile is one scale tile");
 constexpr int kLagA = 4, kLagC = 7;  // least list steps from a K slice's M entry to its A entry; A to C
 constexpr uint32_t KIND_M = 0u, KIND_A = 1u, KIND_C = 2u, KIND_DONE = 3u;
@@ -312,8 +313,8 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
       const int row0 = row_begin + tl * kTR;
       const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
       if (!bar_wait(a, empty + st, ph ^ 1u)) { ok = false; break; }
-      // tiles alternate between the groups: tl + 2 is this group's next tile
-      meta[st] = TileMeta{kind, s, uint32_t(row0), tl + 2 >= nt ? 1u : 0u};
+      // tiles go round the groups: tl + kGroups is this group's next tile
+      meta[st] = TileMeta{kind, s, uint32_t(row0), tl + kGroups >= nt ? 1u : 0u};
       mbar_arrive_expect_tx(full + st, C::SB);
 #pragma unroll
       for (int b = 0; b < C::NB; ++b)
@@ -324,7 +325,7 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     t = t_next;
   }
   if (ok) {
-    // one end marker per consumer group (tiles alternate between the groups)
+    // one end marker per consumer group (tiles go round the groups)
     for (int g = 0; g < kGroups; ++g, ++n) {
       const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
       if (!bar_wait(a, empty + st, ph ^ 1u)) { ok = false; break; }
@@ -635,7 +636,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     return;
   }
 
-  // Consumer warp: group g takes tiles g, g + 2, g + 4, ... of the ring, and
+  // Consumer warp: group g takes tiles g, g + kGroups, ... of the ring, and
   // warp w4 of the group rows 32*w4 .. 32*w4 + 31 of each.  Warps run
   // independently: each waits on the stage itself, keeps its own counts and
   // stores its own rows, so no barrier couples the warps of a group.
@@ -655,7 +656,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   uint32_t run_tiles = 0;  // tiles of the current item this warp has finished
   uint32_t xc = 0;         // per-tile scale exchanges of this warp's group
   for (uint32_t j = 0;; ++j) {
-    const uint32_t n = 2u * j + uint32_t(g);
+    const uint32_t n = uint32_t(kGroups) * j + uint32_t(g);
     const uint32_t st = n % C::NST, ph = (n / C::NST) & 1u;
     if (!warp_bar_wait(a, full + st, ph)) { ok = false; break; }
     const TileMeta tm = meta[st];
