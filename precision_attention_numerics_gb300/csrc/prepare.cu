@@ -406,9 +406,8 @@ __device__ __forceinline__ bool warp_count_wait(const PrepareArgs& a, const uint
 // `flip`, the sign flip is applied as a sign-bit XOR on the raw values (exact,
 // signed zeros included) - only for rows that are not centred, since the
 // flip must follow the centring.
-template <int D, bool BF16>
-__device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint32_t* smask, bool flip,
-                                         uint64_t (&P)[D / 2]) {
+template <int D, bool BF16, bool FLIP>
+__device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint32_t* smask, uint64_t (&P)[D / 2]) {
   using C = FlowCfg<D, BF16>;
   constexpr int PER = BF16 ? 8 : 4, CH = C::ROW_BYTES / 16;  // elements per chunk, chunks per row
   // The per-chunk offsets are recomputed for every tile (an opaque copy of
@@ -419,7 +418,7 @@ __device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint
   auto chunk = [&](int q) -> uint4 {
     const int box = q / 8, cq = q % 8;
     uint4 u = *reinterpret_cast<const uint4*>(rowp + box * (kTR * 128) + ((cq ^ r7) << 4));
-    if (flip) {
+    if constexpr (FLIP) {
       const uint4 m = *reinterpret_cast<const uint4*>(smask + 4 * q);
       u.x ^= m.x; u.y ^= m.y; u.z ^= m.z; u.w ^= m.w;
     }
@@ -447,13 +446,12 @@ __device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint
 // act within each half of the row (packed adds and subtracts).  The order is
 // the method's: s * (x - mu) keeps the sign of a zero difference that
 // s*x - s*mu would lose.  The last stage (h = D/2) is left to the caller.
-template <int D>
-__device__ __forceinline__ void transform_stages(uint64_t (&P)[D / 2], bool center, const uint64_t* nmu,
-                                                 const uint64_t* pmask, bool rotate) {
-  if (center) {
+template <int D, bool CENTER, bool ROTATE>
+__device__ __forceinline__ void transform_stages(uint64_t (&P)[D / 2], const uint64_t* nmu, const uint64_t* pmask) {
+  if constexpr (CENTER) {
 #pragma unroll
     for (int j = 0; j < D / 2; ++j) P[j] = fadd2(P[j], nmu[j]);
-    if (rotate) {
+    if constexpr (ROTATE) {
 #pragma unroll
       for (int j = 0; j < D / 2; j += 2) {
         const uint4 m = *reinterpret_cast<const uint4*>(pmask + j);
@@ -462,7 +460,7 @@ __device__ __forceinline__ void transform_stages(uint64_t (&P)[D / 2], bool cent
       }
     }
   }
-  if (rotate) {
+  if constexpr (ROTATE) {
     const uint64_t neg1 = pack2(-1.0f, -1.0f);
 #pragma unroll
     for (int h = 1; h < D / 2; h <<= 1) {
@@ -723,11 +721,24 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       mu_slice = sr.local;
     }
 
+    // load and transform, each form compiled on its own (no per-chunk tests)
     uint64_t P[D / 2];
-    load_row<D, BF16>(stage, r, smask, rotate && !center, P);
+    if (rotate && !center) {
+      load_row<D, BF16, true>(stage, r, smask, P);
+    } else {
+      load_row<D, BF16, false>(stage, r, smask, P);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty + st);  // the warp's rows are in registers
-    transform_stages<D>(P, center, nmu, pmask, rotate);
+    if (center) {
+      if (rotate) {
+        transform_stages<D, true, true>(P, nmu, pmask);
+      } else {
+        transform_stages<D, true, false>(P, nmu, pmask);
+      }
+    } else if (rotate) {
+      transform_stages<D, false, true>(P, nmu, pmask);
+    }
 
     if (tm.kind == KIND_A) {
       if (valid) run_max = max(run_max, rotate ? rotated_amax_bits<D>(P) : plain_amax_bits<D>(P));
