@@ -623,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ CUtensorMap tv, const Params p) {
   using C = Cfg<D, T>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base by pointer arithmetic on the shared array (an
+  // integer round trip would hide the address space and make every access
+  // through it a generic one)
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = sm;                      // [Q buffer][warpgroup]
   uint8_t* sP = sQ + 4 * C::QB;          // [warpgroup][P buffer]
   uint8_t* sK = sP + 4 * C::PB;

@@ -581,7 +581,10 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   using C = FlowCfg<D, BF16>;
   const PrepareArgs& a = f.a;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base by pointer arithmetic on the shared array (an
+  // integer round trip would hide the address space and make every access
+  // through it a generic one)
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = sm;
   uint8_t* outb = stages + size_t(C::NST) * C::SB;               // [consumer warp][2] staging buffers
   TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(2 * kConsumerWarps) * C::WB);
