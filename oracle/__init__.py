@@ -46,7 +46,7 @@ def lib():
         L.orc_fwht.argtypes = [P, i32]
         L.orc_mean_key.argtypes = [i32, i32, i32, P, P]
         L.orc_prepare.restype = i32
-        L.orc_prepare.argtypes = [i32, i32, i32, i32, i32, i32, u32, P, P, P, P, P, P, P, P, P, P, P]
+        L.orc_prepare.argtypes = [i32, i32, i32, i32, i32, i32, u32, i32, P, P, P, P, P, P, P, P, P, P, P]
         L.orc_attn_exact.restype = i32
         L.orc_attn_exact.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, i32, P, i32, P, i32, P]
         L.orc_attn_quant.restype = i32
@@ -144,11 +144,13 @@ def _dtype_of(a) -> int:
     raise TypeError("inputs are float32 arrays or bf16 bit patterns (uint16)")
 
 
-def prepare(q, k, v, flags: int = 0, signs=None):
+def prepare(q, k, v, flags: int = 0, signs=None, stat_len: int = 0):
     """Operand preparation. Returns dict with q8, k8, v8 (natural layout),
     q_descale [B*Hq], k_descale, v_descale [B*Hkv], k_mean [B*Hkv*d].  With
     TILE_SCALES, q_descale and k_descale hold one descale per 128-row tile:
-    [B*Hq*ntiles] and [B*Hkv*ntiles], ntiles = ceil(N / 128)."""
+    [B*Hq*ntiles] and [B*Hkv*ntiles], ntiles = ceil(N / 128).  stat_len = P
+    (1..N; 0 means N) takes the mean key and the per-(batch, head) scales
+    over the first P tokens of each slice (causal-prefix statistics)."""
     q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
     dt = _dtype_of(q)
     B, Hq, N, d = q.shape
@@ -159,7 +161,7 @@ def prepare(q, k, v, flags: int = 0, signs=None):
     out = dict(q8=np.empty(q.shape, np.uint8), k8=np.empty(k.shape, np.uint8), v8=np.empty(v.shape, np.uint8),
                q_descale=np.empty(B * Hq * nst, np.float32), k_descale=np.empty(B * Hkv * nst, np.float32),
                v_descale=np.empty(B * Hkv, np.float32), k_mean=np.empty(B * Hkv * d, np.float32))
-    rc = lib().orc_prepare(B, Hq, Hkv, N, d, dt, flags, _p(signs), _p(q), _p(k), _p(v), _p(out["q8"]),
+    rc = lib().orc_prepare(B, Hq, Hkv, N, d, dt, flags, int(stat_len), _p(signs), _p(q), _p(k), _p(v), _p(out["q8"]),
                            _p(out["k8"]), _p(out["v8"]), _p(out["q_descale"]), _p(out["k_descale"]),
                            _p(out["v_descale"]), _p(out["k_mean"]))
     _check(rc)

@@ -219,6 +219,15 @@ void orc_fwht(float* x, int d) { fwht(x, d); }
 //      amax = max |x|, qs = 448/amax, descale = amax/448 (float, IEEE
 //      division); amax == 0 gives qs = descale = 1;
 //   5. x8 = E4M3(fl32(x * qs)).
+// Causal-prefix statistics (the "attention-numerics" page, limitations, notes
+// that full-sequence means and scales see future tokens; it defines no
+// generation-safe form, so the plainest one is taken): with stat_len = P,
+// 0 < P <= N, the mean key and the per-(batch, head) amax are taken over the
+// first P tokens of the slice only, and all N tokens are centred and cast with
+// them; a later value above the prefix amax saturates at +-448 by the cast's
+// rule.  P = N (or 0) is the full-sequence preparation.  Per-tile scales are
+// local to their tile and do not change.  The non-finite check still covers
+// every token.
 // Reading of the mean (pages silent on its arithmetic): float sums in a fixed
 // order - per channel, each 128-token chunk summed in token order starting
 // from 0, then the chunk sums added in chunk order - and one IEEE division by
@@ -261,7 +270,8 @@ static void scale_of(float amax, float* qs, float* ds) {
 // (the emulator's per-tile scales that the "attention-numerics" page, method
 // and kernel settings, contrasts with the full-sequence API scales) and
 // descale[t] is tile t's; otherwise one scale for the slice.
-static int prepare_slice(int N, int d, int dtype, const void* X, bool rotate, const int8_t* signs,
+// Without `per_tile` the slice's amax is taken over its first P tokens.
+static int prepare_slice(int N, int P, int d, int dtype, const void* X, bool rotate, const int8_t* signs,
                          const float* mu /* or null */, uint8_t* x8, float* descale, float* transformed_out,
                          bool per_tile = false) {
   std::vector<float> t(size_t(N) * d);
@@ -283,8 +293,9 @@ static int prepare_slice(int N, int d, int dtype, const void* X, bool rotate, co
   const int rows_per_scale = per_tile ? ORC_SCALE_TILE : N;
   for (int j0 = 0, tile = 0; j0 < N; j0 += rows_per_scale, ++tile) {
     const size_t i0 = size_t(j0) * d, i1 = size_t(std::min(N, j0 + rows_per_scale)) * d;
+    const size_t a1 = per_tile ? i1 : size_t(P) * d;  // rows the amax is taken over
     float amax = 0.0f;
-    for (size_t i = i0; i < i1; ++i) amax = std::max(amax, std::fabs(t[i]));
+    for (size_t i = i0; i < a1; ++i) amax = std::max(amax, std::fabs(t[i]));
     float qs, ds;
     scale_of(amax, &qs, &ds);
     descale[tile] = ds;
@@ -294,10 +305,12 @@ static int prepare_slice(int N, int d, int dtype, const void* X, bool rotate, co
   return ORC_OK;
 }
 
-int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags, const int8_t* signs,
+int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags, int stat_len, const int8_t* signs,
                 const void* Q, const void* K, const void* V, uint8_t* q8, uint8_t* k8, uint8_t* v8,
                 float* q_descale, float* k_descale, float* v_descale, float* k_mean) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0 || d <= 0 || (d & (d - 1)) || Hq % Hkv) return ORC_EINVAL;
+  if (stat_len < 0 || stat_len > N) return ORC_EINVAL;
+  const int P = stat_len == 0 ? N : stat_len;  // tokens the mean and the slice scales see
   const bool rotate = flags & ORC_ROTATE, center = flags & ORC_CENTER_K, tiles = flags & ORC_TILE_SCALES;
   if (rotate && !signs) return ORC_EINVAL;
   const size_t es = dtype == ORC_BF16 ? 2 : 4;
@@ -310,7 +323,7 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
   parallel_for(nq + 2 * nk, nthreads(), [&](int64_t u) {
     int rc;
     if (u < nq) {
-      rc = prepare_slice(N, d, dtype, static_cast<const char*>(Q) + es * slice * u, rotate, signs, nullptr,
+      rc = prepare_slice(N, P, d, dtype, static_cast<const char*>(Q) + es * slice * u, rotate, signs, nullptr,
                          q8 + slice * u, q_descale + per * u, nullptr, tiles);
     } else if (u < nq + nk) {
       int64_t g = u - nq;
@@ -318,12 +331,12 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
       float* mu = nullptr;
       if (center) {
         mu = &mus[size_t(g) * d];
-        orc_mean_key(N, d, dtype, Kh, mu);
+        orc_mean_key(P, d, dtype, Kh, mu);  // the mean of the first P tokens
       }
-      rc = prepare_slice(N, d, dtype, Kh, rotate, signs, mu, k8 + slice * g, k_descale + per * g, nullptr, tiles);
+      rc = prepare_slice(N, P, d, dtype, Kh, rotate, signs, mu, k8 + slice * g, k_descale + per * g, nullptr, tiles);
     } else {
       int64_t g = u - nq - nk;
-      rc = prepare_slice(N, d, dtype, static_cast<const char*>(V) + es * slice * g, false, nullptr, nullptr,
+      rc = prepare_slice(N, P, d, dtype, static_cast<const char*>(V) + es * slice * g, false, nullptr, nullptr,
                          v8 + slice * g, v_descale + g, nullptr);
     }
     if (rc != ORC_OK) status.store(rc);
