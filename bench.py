@@ -185,7 +185,7 @@ def dist_env():
 # oracle (CPU) sample: the CPU baseline and the reference arm
 # ---------------------------------------------------------------------------
 
-def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0):
+def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0, stat_len=0):
     """Oracle prepare of one (batch, KV group) and quantised emulation of the
     given query rows of its query heads.  Returns (seconds, flops, threads)."""
     import oracle
@@ -195,7 +195,7 @@ def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0):
     vs = v[b:b + 1, heads_group:heads_group + 1]
     N, d = WL["N"], WL["d"]
     t0 = time.perf_counter()
-    prep = oracle.prepare(qs, ks, vs, flags=oracle.ROTATE | oracle.CENTER_K, signs=signs)
+    prep = oracle.prepare(qs, ks, vs, flags=oracle.ROTATE | oracle.CENTER_K, signs=signs, stat_len=stat_len)
     oracle.attn_quant(prep, (1, G, 1, N, d), oracle.ROTATE | oracle.CENTER_K, WL["S"], 1, True, WL["kv_tile"],
                       rows=rows)
     dt = time.perf_counter() - t0
@@ -348,7 +348,7 @@ def run_ours(args):
     Vh = torch.from_numpy(v_np).view(torch.bfloat16).pin_memory()
     Q, K, V = Qh.to(dev), Kh.to(dev), Vh.to(dev)
     signs = torch.from_numpy(signs_np).to(dev)
-    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, flags, signs)
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, flags, signs, args.stat_len)
     bufs = aq.alloc_prepared(desc, device=dev)
     O = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev)
     Oh = torch.empty((B, Hq, N, d), dtype=torch.bfloat16).pin_memory()
@@ -447,7 +447,7 @@ def run_ours(args):
         cpu = None
         if not args.no_cpu_baseline:
             rows_s = sample_rows(args.cpu_rows)
-            dt, fl, thr = oracle_sample(q_np, k_np, v_np, signs_np, rows_s)
+            dt, fl, thr = oracle_sample(q_np, k_np, v_np, signs_np, rows_s, stat_len=args.stat_len)
             cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                    "sample": (f"oracle prepare of one (batch, KV group) (4 query heads, 1 KV head) + quantised "
                               f"emulation of {len(rows_s)} query rows in [N/2, N) of those heads; "
@@ -456,7 +456,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
-            "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "rotate": True, "center_k": True, "scales": "per-tile (128 tokens)" if args.scales == "tile" else "per (batch, head)", "in_dtype": "bf16",
+            "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "rotate": True, "center_k": True, "scales": "per-tile (128 tokens)" if args.scales == "tile" else "per (batch, head)",
+                       "statistics": f"first {args.stat_len} tokens" if args.stat_len else "full sequence", "in_dtype": "bf16",
                        "out_dtype": "bf16", "step": "attnq_prepare + attnq_fwd",
                        "l2": "inputs 805 MB per step > 129 MB L2; no flush",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -499,6 +500,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--scales", choices=["slice", "tile"], default="slice",
                     help="Q/K scales per (batch, head) (the timed workload) or per 128-token tile")
+    ap.add_argument("--stat-len", type=int, default=0,
+                    help="causal-prefix statistics: mean key and slice scales over the first P tokens (0: all N)")
     ap.add_argument("--B", type=int, default=WL["B"], help="smaller batch for profiling captures")
     ap.add_argument("--Hq", type=int, default=WL["Hq"])
     ap.add_argument("--Hkv", type=int, default=WL["Hkv"])

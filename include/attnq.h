@@ -79,12 +79,23 @@ enum { ATTNQ_KV_FORWARD = 0, ATTNQ_KV_REVERSE = 1 };
  *                   one scale per (batch, head).
  * signs: DEVICE pointer to d int8 values, each +1 or -1; required when
  * ATTNQ_ROTATE is set, ignored otherwise.
+ * stat_len: 0 (full sequence), or P in 1..N: causal-prefix statistics.  The
+ *   mean key and the one-per-(batch, head) amax of attnq_prepare are taken
+ *   over the first P tokens of each slice only, and all N tokens are centred
+ *   and cast with them; a later value above the prefix amax saturates at
+ *   +-448 by the cast's rule.  The "attention-numerics" page (limitations)
+ *   notes that full-sequence means and scales see future tokens; this is the
+ *   generation-safe form when the first P tokens are a prompt known before
+ *   the rest.  Per-tile Q/K scales (ATTNQ_TILE_SCALES) are local to their
+ *   tile and ignore it; V's scale and the mean key still use it.
+ *   A zero-initialised descriptor has stat_len = 0.
  */
 typedef struct {
   int32_t B, Hq, Hkv, N, d;
   int32_t in_dtype;
   uint32_t flags;
   const int8_t* signs;
+  int32_t stat_len;
 } attnq_desc;
 
 /*
@@ -130,12 +141,15 @@ size_t attnq_prepare_workspace(const attnq_desc* desc);
  * Operand preparation [AN], [RR]: for every (batch, head) slice of Q, K, V
  *   1. upcast to fp32;
  *   2. K only, with ATTNQ_CENTER_K: subtract the mean key mu (fp32; per
- *      channel, 128-token chunks summed in token order, chunk sums added in
- *      chunk order, one IEEE division by N);
+ *      channel, 128-token chunks of the first P tokens summed in token
+ *      order, chunk sums added in chunk order, one IEEE division by P;
+ *      P = desc->stat_len, or N when it is 0);
  *   3. Q and K only, with ATTNQ_ROTATE: x <- FWHT(signs * x), unnormalised,
  *      butterfly stages h = 1, 2, ..., d/2;
- *   4. amax = max |x| over the slice; descale = amax/448 and qs = 448/amax
- *      (IEEE fp32 division; 1 and 1 when amax == 0);
+ *   4. amax = max |x| over the first P tokens of the slice (over each
+ *      128-token tile for Q and K with ATTNQ_TILE_SCALES); descale =
+ *      amax/448 and qs = 448/amax (IEEE fp32 division; 1 and 1 when
+ *      amax == 0);
  *   5. x8 = E4M3 code of fl32(x * qs), round-to-nearest-even, saturating.
  * Q, K, V: DEVICE, in_dtype elements, [B,H,N,d].  q8 [B,Hq,N,d], k8
  * [B,Hkv,N,d]: DEVICE uint8 E4M3 codes.  v8: [B,Hkv,N,d], or
@@ -143,8 +157,9 @@ size_t attnq_prepare_workspace(const attnq_desc* desc);
  * optional mean key) as DEVICE pointers.  workspace: DEVICE, at least
  * attnq_prepare_workspace(desc) bytes, 256-byte aligned; its contents need no
  * initialisation and are garbage afterwards.  A non-finite value in an input
- * slice (or produced by its transform) sets ATTNQ_ENONFINITE in the device
- * status; outputs are then unspecified.
+ * slice (or produced by its transform), inside the prefix or after it, sets
+ * ATTNQ_ENONFINITE in the device status; outputs are then unspecified.
+ * Returns ATTNQ_EINVAL for stat_len < 0 or > N.
  */
 attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K, const void* V, uint8_t* q8,
                            uint8_t* k8, uint8_t* v8, const attnq_scales* out, void* workspace, size_t ws_bytes,

@@ -39,7 +39,7 @@ class AttnqError(RuntimeError):
 
 class _Desc(C.Structure):
     _fields_ = [("B", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("N", C.c_int32), ("d", C.c_int32),
-                ("in_dtype", C.c_int32), ("flags", C.c_uint32), ("signs", C.c_void_p)]
+                ("in_dtype", C.c_int32), ("flags", C.c_uint32), ("signs", C.c_void_p), ("stat_len", C.c_int32)]
 
 
 class _Scales(C.Structure):
@@ -49,7 +49,9 @@ class _Scales(C.Structure):
 
 @dataclass
 class AttnqDesc:
-    """Mirror of attnq_desc; `signs` is a device int8 tensor of d values or None."""
+    """Mirror of attnq_desc; `signs` is a device int8 tensor of d values or None;
+    `stat_len` = P takes the mean key and the per-(batch, head) scales over the
+    first P tokens (0: all N)."""
     B: int
     Hq: int
     Hkv: int
@@ -58,10 +60,11 @@ class AttnqDesc:
     in_dtype: int = ATTNQ_BF16
     flags: int = ATTNQ_VT_LAYOUT
     signs: Optional[object] = None
+    stat_len: int = 0
 
     def _c(self) -> _Desc:
         return _Desc(self.B, self.Hq, self.Hkv, self.N, self.d, self.in_dtype, self.flags,
-                     None if self.signs is None else self.signs.data_ptr())
+                     None if self.signs is None else self.signs.data_ptr(), self.stat_len)
 
 
 @dataclass

@@ -59,6 +59,7 @@ attnq_status check_desc(const attnq_desc* d) {
   if (d->Hq % d->Hkv != 0) return ATTNQ_EINVAL;
   if ((d->flags & ~uint32_t(ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT | ATTNQ_TILE_SCALES)) != 0)
     return ATTNQ_EINVAL;
+  if (d->stat_len < 0 || d->stat_len > d->N) return ATTNQ_EINVAL;
   if (d->d != 64 && d->d != 128) return ATTNQ_EUNSUPPORTED;
   // grid.y of the prepare passes and int32 indices of rows
   const int64_t nslices = int64_t(d->B) * d->Hq + 2 * int64_t(d->B) * d->Hkv;
@@ -202,13 +203,38 @@ CUresult encode_tiled_3d(CUtensorMap* map, const void* base, uint64_t dim0, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+namespace {
+
+// Kernel arguments of one preparation (the workspace is carved by the caller).
+PrepareArgs prepare_args(const attnq_desc* desc, const void* Q, const void* K, const void* V, uint8_t* q8,
+                         uint8_t* k8, uint8_t* v8, const attnq_scales* out, int dev) {
+  PrepareArgs a{};
+  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d;
+  a.P = desc->stat_len > 0 ? desc->stat_len : desc->N;
+  a.bf16 = desc->in_dtype == ATTNQ_BF16;
+  a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
+  a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
+  a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
+  a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
+  a.signs = desc->signs;
+  a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
+  a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
+  a.ldv = attnq_vt_ld(desc->N);
+  a.status = g_status_ptr[dev];
+  a.num_sms = g_num_sms[dev];
+  a.wait_ns = g_wait_ns.load();
+  return a;
+}
+
+}  // namespace
+
 }  // namespace attnq
 
 using namespace attnq;
 
 extern "C" {
 
-int32_t attnq_version(void) { return 100; }
+int32_t attnq_version(void) { return 200; }
 
 const char* attnq_status_string(attnq_status s) {
   switch (s) {
@@ -260,20 +286,7 @@ attnq_status attnq_prepare(const attnq_desc* desc, const void* Q, const void* K,
   int dev;
   st = device_setup(&dev);
   if (st != ATTNQ_OK) return st;
-  PrepareArgs a{};
-  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d;
-  a.bf16 = desc->in_dtype == ATTNQ_BF16;
-  a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
-  a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
-  a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
-  a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
-  a.signs = desc->signs;
-  a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
-  a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
-  a.ldv = attnq_vt_ld(desc->N);
-  a.status = g_status_ptr[dev];
-  a.num_sms = g_num_sms[dev];
-  a.wait_ns = g_wait_ns.load();
+  PrepareArgs a = prepare_args(desc, Q, K, V, q8, k8, v8, out, dev);
   carve_prepare_workspace(a, workspace);
   const NvtxRange range("attnq_prepare");
   return from_cuda(launch_prepare(a, stream));
@@ -297,20 +310,7 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
   if (st != ATTNQ_OK) return st;
   void* scratch = nullptr;
   if (static_scratch_address(&scratch) != cudaSuccess) return ATTNQ_ECUDA;
-  PrepareArgs a{};
-  a.B = desc->B; a.Hq = desc->Hq; a.Hkv = desc->Hkv; a.N = desc->N; a.d = desc->d;
-  a.bf16 = desc->in_dtype == ATTNQ_BF16;
-  a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
-  a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
-  a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
-  a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
-  a.signs = desc->signs;
-  a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
-  a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
-  a.ldv = attnq_vt_ld(desc->N);
-  a.status = g_status_ptr[dev];
-  a.num_sms = g_num_sms[dev];
-  a.wait_ns = g_wait_ns.load();
+  PrepareArgs a = prepare_args(desc, Q, K, V, q8, k8, v8, out, dev);
   carve_prepare_workspace(a, scratch);   // the launch itself clears the counters it uses
   const NvtxRange range("attnq_prepare");
   return from_cuda(launch_prepare(a, stream));

@@ -14,6 +14,7 @@ constexpr int kScaleTile = 128;
 
 struct PrepareArgs {
   int B, Hq, Hkv, N, d;
+  int P;              // tokens the mean key and the slice scales are taken over (1..N)
   int bf16;           // input element type: 1 bf16, 0 fp32
   int rotate, center, vt;
   int tiles;          // per-tile Q/K scales

@@ -24,6 +24,12 @@
 // cannot deadlock, and
 // it needs no co-residency.
 //
+// Causal-prefix statistics (the "attention-numerics" page, limitations: full-
+// sequence means and scales see future tokens): with P < N the M and A passes
+// cover only the first P tokens of a slice (their later items are empty and
+// skipped), the mean divides by P, and the C pass casts all N tokens with the
+// prefix's scale, checking the later tokens for non-finite values itself.
+//
 // CTA: warp 8 claims items and streams their tiles into a ring of shared
 // memory stages with TMA (128-byte swizzle, rows beyond N read as zero;
 // warps 9-11 only complete its warpgroup for the register split);
@@ -201,6 +207,7 @@ __global__ void k_flow_init(PrepareArgs a) {
 struct Flow {
   PrepareArgs a;
   int tiles_per_slice, items_per_slice;
+  int tiles_stat;  // tiles holding the first P tokens (the M and A passes)
 };
 
 __device__ __forceinline__ void raise_abort(const PrepareArgs& a) {
@@ -307,7 +314,13 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     const SliceRef r = slice_ref(a, int(s));
     const CUtensorMap* map = in_maps[r.tensor];
     const int row_begin = int(item) * kTR * kTilesPerItem;
-    const int nt = min(kTilesPerItem, (a.N - row_begin + kTR - 1) / kTR);
+    // the M and A passes read only the first P tokens: their later items are empty
+    const int lim = kind == KIND_C ? a.N : a.P;
+    const int nt = min(kTilesPerItem, (lim - row_begin + kTR - 1) / kTR);
+    if (nt <= 0) {
+      t = atomicAdd(a.ctl + CTL_TICKET, 1u);
+      continue;
+    }
     for (int tl = 0; tl < nt && ok; ++tl, ++n) {
       if (tl == (nt > 2 ? nt - 2 : 0)) t_next = atomicAdd(a.ctl + CTL_TICKET, 1u);
       const int row0 = row_begin + tl * kTR;
@@ -538,18 +551,19 @@ __device__ __forceinline__ void row_codes(const uint64_t (&P)[D / 2], float qs, 
   }
 }
 
-// Mean key of K slice `sl` from its chunk sums: per channel, the chunk sums
-// added in chunk order, then one division by N.  Lane l owns channels
-// l, l + 32, ...; the loads run eight chunks ahead of the ordered adds.
+// Mean key of K slice `sl` from the chunk sums of its first P tokens: per
+// channel, the `chunks` sums added in chunk order, then one division by P.
+// Lane l owns channels l, l + 32, ...; the loads run eight chunks ahead of the
+// ordered adds.
 template <int D>
-__device__ __forceinline__ void finish_mean(const PrepareArgs& a, int tiles_per_slice, int sl, int lane) {
+__device__ __forceinline__ void finish_mean(const PrepareArgs& a, int tiles_per_slice, int chunks, int sl, int lane) {
   constexpr int CPL = D / 32;
   const float* base = a.mean_part + int64_t(sl) * tiles_per_slice * D + lane;
   float tot[CPL];
 #pragma unroll
   for (int i = 0; i < CPL; ++i) tot[i] = 0.0f;
   int k = 0;
-  for (; k + 8 <= tiles_per_slice; k += 8) {
+  for (; k + 8 <= chunks; k += 8) {
     float v[8][CPL];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
@@ -560,12 +574,12 @@ __device__ __forceinline__ void finish_mean(const PrepareArgs& a, int tiles_per_
 #pragma unroll
       for (int i = 0; i < CPL; ++i) tot[i] = __fadd_rn(tot[i], v[u][i]);
   }
-  for (; k < tiles_per_slice; ++k)
+  for (; k < chunks; ++k)
 #pragma unroll
     for (int i = 0; i < CPL; ++i) tot[i] = __fadd_rn(tot[i], __ldcg(base + int64_t(k) * D + 32 * i));
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
-    const float mu = __fdiv_rn(tot[i], float(a.N));
+    const float mu = __fdiv_rn(tot[i], float(a.P));
     a.mu[sl * D + lane + 32 * i] = mu;
     if (a.k_mean) a.k_mean[sl * D + lane + 32 * i] = mu;
   }
@@ -646,6 +660,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   uint64_t* nmu = nmu_all + warp * (D / 2);
   uint8_t* obuf = outb + size_t(2 * warp) * C::WB;
   const uint32_t tiles = uint32_t(f.tiles_per_slice);
+  const uint32_t stat_tiles = uint32_t(f.tiles_stat);  // M and A tiles of a slice
   int mu_slice = -1;   // K slice whose -mu is in nmu
   int qs_slice = -1;   // slice whose scale is in qs
   float qs = 0.0f;
@@ -666,7 +681,8 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     const int s = int(tm.slice);
     const SliceRef sr = slice_ref(a, s);
     const int row0 = int(tm.row0);
-    const bool valid = row0 + r < a.N;
+    // rows the pass covers: every token for the cast, the first P for M and A
+    const bool valid = row0 + r < (tm.kind == KIND_C ? a.N : a.P);
     const bool qk = sr.tensor < 2;
     const bool rotate = a.rotate && qk, center = a.center && sr.tensor == 1;
 
@@ -675,7 +691,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       // thread r owns channel r (warps past the last channel only release)
       const bool has = 32 * w4 < D;
       if (has) {
-        const int rows = min(kTR, a.N - row0);
+        const int rows = min(kTR, a.P - row0);
         const int byte = r * C::ES, box = byte / 128, cq = (byte % 128) / 16, off = byte % 16;
         // loads in batches of 16 (independent), then the adds in token order
         float part = 0.0f;
@@ -703,11 +719,12 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       __threadfence();
       __syncwarp();
       uint32_t fin = 0;
-      if (lane == 0) fin = atomicAdd(a.m_done + sr.local, run_tiles) + run_tiles == tiles * uint32_t(D / 32) ? 1u : 0u;
+      if (lane == 0)
+        fin = atomicAdd(a.m_done + sr.local, run_tiles) + run_tiles == stat_tiles * uint32_t(D / 32) ? 1u : 0u;
       run_tiles = 0;
       if (__shfl_sync(0xffffffffu, fin, 0) != 0u) {
         __threadfence();
-        finish_mean<D>(a, f.tiles_per_slice, sr.local, lane);
+        finish_mean<D>(a, f.tiles_per_slice, f.tiles_stat, sr.local, lane);
         __threadfence();
         __syncwarp();
         if (lane == 0) flag_set(a.mu_ready + sr.local);
@@ -784,7 +801,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     } else {
       if (qs_slice != s) {
         // every A tile of the slice has added its amax (acquire on the count)
-        if (!warp_count_wait(a, a.a_done + s, tiles * 4u)) { ok = false; break; }
+        if (!warp_count_wait(a, a.a_done + s, stat_tiles * 4u)) { ok = false; break; }
         qs_bits = __ldcg(a.amax_bits + s);
         float ds;
         scale_from_amax(qs_bits, qs, ds);
@@ -796,6 +813,12 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
         scale_from_amax(qs_bits, q2, ds);
         (sr.tensor == 0 ? a.q_ds : sr.tensor == 1 ? a.k_ds : a.v_ds)[sr.local] = ds;
         if (qs_bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
+      }
+      // tokens after the prefix took no part in the amax: check them here
+      if (row0 + kTR > a.P) {
+        const bool bad = valid && row0 + r >= a.P &&
+                         (rotate ? rotated_amax_bits<D>(P) : plain_amax_bits<D>(P)) >= 0x7F800000u;
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, DEV_NONFINITE);
       }
     }
     if (rotate) final_stage<D>(P);
@@ -874,6 +897,7 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   f.a = a;
   f.tiles_per_slice = (a.N + kTR - 1) / kTR;
   f.items_per_slice = (f.tiles_per_slice + kTilesPerItem - 1) / kTilesPerItem;
+  f.tiles_stat = (a.P + kTR - 1) / kTR;
   k_flow_init<<<1, 256, 0, st>>>(a);
   auto kern = k_prepare<D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));

@@ -23,12 +23,12 @@ def dev(a: np.ndarray) -> torch.Tensor:
     return t.cuda()
 
 
-def gpu_prepare(q, k, v, flags: int, signs=None, vt: bool = True):
+def gpu_prepare(q, k, v, flags: int, signs=None, vt: bool = True, stat_len: int = 0):
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
     in_dtype = aq.ATTNQ_BF16 if q.dtype == np.uint16 else aq.ATTNQ_F32
     st = None if signs is None else torch.from_numpy(np.ascontiguousarray(signs, dtype=np.int8)).cuda()
-    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, in_dtype, flags | (aq.ATTNQ_VT_LAYOUT if vt else 0), st)
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, in_dtype, flags | (aq.ATTNQ_VT_LAYOUT if vt else 0), st, stat_len)
     bufs = aq.alloc_prepared(desc)
     Q, K, V = dev(q), dev(k), dev(v)
     aq.attnq_prepare(desc, Q, K, V, bufs.q8, bufs.k8, bufs.v8, bufs.scales, bufs.workspace)

@@ -2,6 +2,9 @@
 include/attnq.h declares, and its host-only helpers behave as documented.
 No compute call is made here."""
 import ctypes as C
+import os
+import shutil
+import subprocess
 
 import numpy as np
 import pytest
@@ -46,8 +49,9 @@ def test_hadamard_signs_follow_splitmix64(aq, seed):
 def test_argument_checks_before_any_cuda_call(aq):
     L = aq.load_library()
     bad = [aq.AttnqDesc(1, 4, 3, 16, 64), aq.AttnqDesc(1, 1, 1, 16, 96), aq.AttnqDesc(0, 1, 1, 16, 64),
-           aq.AttnqDesc(1, 1, 1, 0, 64), aq.AttnqDesc(1, 1, 1, 16, 64, flags=64)]
-    want = [1, 2, 1, 1, 1]
+           aq.AttnqDesc(1, 1, 1, 0, 64), aq.AttnqDesc(1, 1, 1, 16, 64, flags=64),
+           aq.AttnqDesc(1, 1, 1, 16, 64, stat_len=-1), aq.AttnqDesc(1, 1, 1, 16, 64, stat_len=17)]
+    want = [1, 2, 1, 1, 1, 1, 1]
     for desc, code in zip(bad, want):
         d = desc._c()
         assert L.attnq_prepare_workspace(C.byref(d)) == 0
@@ -62,3 +66,24 @@ def test_workspace_size_grows_with_centring(aq):
     w0, w1 = aq.attnq_prepare_workspace(d0), aq.attnq_prepare_workspace(d1)
     assert 0 < w0 < w1
     assert w1 - w0 >= 2 * 8 * (32768 // 128) * 128 * 4
+
+
+def test_descriptor_layout_matches_the_header(aq, tmp_path):
+    """The ctypes mirrors have the C structs' sizes and field offsets."""
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = tmp_path / "layout.c"
+    src.write_text(
+        "#include <stdio.h>\n#include \"attnq.h\"\n"
+        "int main(void) { printf(\"%zu %zu %zu %zu\\n\", sizeof(attnq_desc), offsetof(attnq_desc, signs),"
+        " offsetof(attnq_desc, stat_len), sizeof(attnq_scales)); return 0; }\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(root, "include"), "-I", cuda_inc, str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    from precision_attention_numerics_gb300 import binding
+    want = [C.sizeof(binding._Desc), binding._Desc.signs.offset, binding._Desc.stat_len.offset,
+            C.sizeof(binding._Scales)]
+    assert got == want
