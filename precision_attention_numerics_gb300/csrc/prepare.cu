@@ -29,6 +29,7 @@
 // cover only the first P tokens of a slice (their later items are empty and
 // skipped), the mean divides by P, and the C pass casts all N tokens with the
 // prefix's scale, checking the later tokens for non-finite values itself.
+// That form is its own instance, so the full-sequence kernel carries none of it.
 //
 // CTA: warp 8 claims items and streams their tiles into a ring of shared
 // memory stages with TMA (128-byte swizzle, rows beyond N read as zero;
@@ -288,7 +289,8 @@ __device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
 }
 
 // ---- producer -------------------------------------------------------------
-template <int D, bool BF16>
+// PREFIX: statistics over the first P < N tokens (the M and A entries stop there).
+template <int D, bool BF16, bool PREFIX>
 __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8_t* stages, TileMeta* meta,
                          uint64_t* full, uint64_t* empty) {
   using C = FlowCfg<D, BF16>;
@@ -315,9 +317,9 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     const CUtensorMap* map = in_maps[r.tensor];
     const int row_begin = int(item) * kTR * kTilesPerItem;
     // the M and A passes read only the first P tokens: their later items are empty
-    const int lim = kind == KIND_C ? a.N : a.P;
+    const int lim = (PREFIX && kind != KIND_C) ? a.P : a.N;
     const int nt = min(kTilesPerItem, (lim - row_begin + kTR - 1) / kTR);
-    if (nt <= 0) {
+    if (PREFIX && nt <= 0) {
       t = atomicAdd(a.ctl + CTL_TICKET, 1u);
       continue;
     }
@@ -586,7 +588,9 @@ __device__ __forceinline__ void finish_mean(const PrepareArgs& a, int tiles_per_
 }
 
 // ---- the persistent kernel ----------------------------------------------------
-template <int D, bool BF16>
+// PREFIX is the causal-prefix form (P < N); without it the kernel is the
+// full-sequence one and carries no prefix code.
+template <int D, bool BF16, bool PREFIX>
 __global__ void __launch_bounds__(kFlowThreads, 1)
     k_prepare(const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
               const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_q,
@@ -646,7 +650,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       tma_prefetch_desc(&in_k);
       tma_prefetch_desc(&in_v);
       const CUtensorMap* maps[3] = {&in_q, &in_k, &in_v};
-      producer<D, BF16>(f, maps, stages, meta, full, empty);
+      producer<D, BF16, PREFIX>(f, maps, stages, meta, full, empty);
     }
     return;
   }
@@ -661,6 +665,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   uint8_t* obuf = outb + size_t(2 * warp) * C::WB;
   const uint32_t tiles = uint32_t(f.tiles_per_slice);
   const uint32_t stat_tiles = uint32_t(f.tiles_stat);  // M and A tiles of a slice
+  const int plen = PREFIX ? a.P : a.N;                 // tokens the M and A passes cover
   int mu_slice = -1;   // K slice whose -mu is in nmu
   int qs_slice = -1;   // slice whose scale is in qs
   float qs = 0.0f;
@@ -682,7 +687,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     const SliceRef sr = slice_ref(a, s);
     const int row0 = int(tm.row0);
     // rows the pass covers: every token for the cast, the first P for M and A
-    const bool valid = row0 + r < (tm.kind == KIND_C ? a.N : a.P);
+    const bool valid = row0 + r < (PREFIX && tm.kind != KIND_C ? plen : a.N);
     const bool qk = sr.tensor < 2;
     const bool rotate = a.rotate && qk, center = a.center && sr.tensor == 1;
 
@@ -691,7 +696,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       // thread r owns channel r (warps past the last channel only release)
       const bool has = 32 * w4 < D;
       if (has) {
-        const int rows = min(kTR, a.P - row0);
+        const int rows = min(kTR, plen - row0);
         const int byte = r * C::ES, box = byte / 128, cq = (byte % 128) / 16, off = byte % 16;
         // loads in batches of 16 (independent), then the adds in token order
         float part = 0.0f;
@@ -815,8 +820,8 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
         if (qs_bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
       }
       // tokens after the prefix took no part in the amax: check them here
-      if (row0 + kTR > a.P) {
-        const bool bad = valid && row0 + r >= a.P &&
+      if (PREFIX && row0 + kTR > plen) {
+        const bool bad = valid && row0 + r >= plen &&
                          (rotate ? rotated_amax_bits<D>(P) : plain_amax_bits<D>(P)) >= 0x7F800000u;
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, DEV_NONFINITE);
       }
@@ -899,7 +904,7 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   f.items_per_slice = (f.tiles_per_slice + kTilesPerItem - 1) / kTilesPerItem;
   f.tiles_stat = (a.P + kTR - 1) / kTR;
   k_flow_init<<<1, 256, 0, st>>>(a);
-  auto kern = k_prepare<D, BF16>;
+  auto kern = a.P < a.N ? k_prepare<D, BF16, true> : k_prepare<D, BF16, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
