@@ -21,6 +21,7 @@ from . import build as _build
 ROTATE = 1
 CENTER_K = 2
 TILE_SCALES = 8
+I8QK = 16
 SCALE_TILE = 128
 F32 = 0
 BF16 = 1
@@ -41,6 +42,7 @@ def lib():
         L.orc_e4m3_encode.restype = C.c_uint8
         L.orc_e4m3_encode.argtypes = [f32]
         L.orc_e4m3_encode_array.argtypes = [P, P, i64]
+        L.orc_int8_encode_array.argtypes = [P, P, i64]
         L.orc_e4m3_encode_bits_range.argtypes = [C.c_uint64, i64, P]
         L.orc_double_to_bf16_array.argtypes = [P, P, i64]
         L.orc_fwht.argtypes = [P, i32]
@@ -100,6 +102,14 @@ def e4m3_encode(x) -> np.ndarray:
     return out
 
 
+def int8_encode(x) -> np.ndarray:
+    """Symmetric INT8 codes: nearest integer, ties to even, saturated to +-127."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.int8)
+    lib().orc_int8_encode_array(_p(x), _p(out), x.size)
+    return out
+
+
 def e4m3_encode_bits(start: int, count: int) -> np.ndarray:
     """Codes for every float32 bit pattern start .. start+count-1."""
     out = np.empty(count, dtype=np.uint8)
@@ -150,7 +160,9 @@ def prepare(q, k, v, flags: int = 0, signs=None, stat_len: int = 0):
     TILE_SCALES, q_descale and k_descale hold one descale per 128-row tile:
     [B*Hq*ntiles] and [B*Hkv*ntiles], ntiles = ceil(N / 128).  stat_len = P
     (1..N; 0 means N) takes the mean key and the per-(batch, head) scales
-    over the first P tokens of each slice (causal-prefix statistics)."""
+    over the first P tokens of each slice (causal-prefix statistics).  With
+    I8QK, q8 and k8 are int8 arrays of symmetric INT8 codes (descale =
+    amax / 127); v8 stays E4M3."""
     q, k, v = (np.ascontiguousarray(a) for a in (q, k, v))
     dt = _dtype_of(q)
     B, Hq, N, d = q.shape
@@ -165,6 +177,8 @@ def prepare(q, k, v, flags: int = 0, signs=None, stat_len: int = 0):
                            _p(out["k8"]), _p(out["v8"]), _p(out["q_descale"]), _p(out["k_descale"]),
                            _p(out["v_descale"]), _p(out["k_mean"]))
     _check(rc)
+    if flags & I8QK:
+        out["q8"], out["k8"] = out["q8"].view(np.int8), out["k8"].view(np.int8)
     return out
 
 
@@ -191,7 +205,8 @@ def attn_exact(q, k, v, causal: bool = True, bh_list=None, rows=None) -> np.ndar
 
 def attn_quant(prep, shape, flags: int, S: float, kv_order: int, causal: bool, kv_tile: int, k_sink: int = 4,
                mode: int = 0, bh_list=None, rows=None):
-    """Quantised forward emulation on prepared E4M3 operands (natural layout).
+    """Quantised forward emulation on prepared E4M3 operands (natural layout;
+    with I8QK in flags, INT8 Q and K codes and an exact integer q.k).
 
     shape = (B, Hq, Hkv, N, d).  Returns (O double [n_bh, n_rows, d],
     underflow uint64 [n_bh, 2])."""

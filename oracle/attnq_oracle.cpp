@@ -89,6 +89,26 @@ uint8_t e4m3_encode(float x) {
 
 inline double dec(uint8_t c) { return tab().dec[c]; }
 
+// ---------------------------------------------------------------------------
+// Symmetric INT8 code of a float (the Q.K format of the INT8-QK / FP8-PV
+// kernel that the "attention-numerics" page, method and kernel settings,
+// runs): the nearest integer, ties to even, saturated to [-127, 127].  The
+// page names only the format; -128 is left unused so the code range is
+// symmetric like the max-based scale that feeds it.  NaN gives 0 (non-finite
+// inputs are rejected before any cast).
+// ---------------------------------------------------------------------------
+int8_t int8_encode(float y) {
+  if (std::isnan(y)) return 0;
+  const double a = double(y);
+  if (a >= 127.0) return 127;
+  if (a <= -127.0) return -127;
+  const double f = std::floor(a);
+  const double frac = a - f;  // exact: a and f are within 2^8 of each other
+  long k = long(f);
+  if (frac > 0.5 || (frac == 0.5 && k % 2 != 0)) k += 1;
+  return int8_t(k);
+}
+
 // bf16 bit pattern -> float (exact)
 inline float bf16_to_float(uint16_t u) {
   uint32_t b = uint32_t(u) << 16;
@@ -168,7 +188,7 @@ constexpr double LOG2E = 1.4426950408889634073599246810018921;  // 1/ln 2
 extern "C" {
 
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_ENONFINITE = 4 };
-enum { ORC_ROTATE = 1u, ORC_CENTER_K = 2u, ORC_TILE_SCALES = 8u };
+enum { ORC_ROTATE = 1u, ORC_CENTER_K = 2u, ORC_TILE_SCALES = 8u, ORC_I8QK = 16u };
 // Scale tile of the per-tile variant: 128 consecutive tokens of one (batch,
 // head), aligned at token 0.
 constexpr int ORC_SCALE_TILE = 128;
@@ -179,6 +199,9 @@ int orc_get_threads(void) { return nthreads(); }
 
 double orc_e4m3_decode(uint8_t c) { return dec(c); }
 uint8_t orc_e4m3_encode(float x) { return e4m3_encode(x); }
+void orc_int8_encode_array(const float* x, int8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = int8_encode(x[i]);
+}
 
 void orc_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
   const int64_t blk = 1 << 20;
@@ -255,13 +278,14 @@ int orc_mean_key(int N, int d, int dtype, const void* K_head, float* mu) {
   return ORC_OK;
 }
 
-// qs = 448/amax and descale = amax/448 (IEEE division); amax = 0 gives 1, 1.
-static void scale_of(float amax, float* qs, float* ds) {
+// qs = top/amax and descale = amax/top (IEEE division), top = 448 for E4M3
+// and 127 for INT8 codes; amax = 0 gives 1, 1.
+static void scale_of(float amax, float top, float* qs, float* ds) {
   *qs = 1.0f;
   *ds = 1.0f;
   if (amax > 0.0f) {
-    *qs = 448.0f / amax;
-    *ds = amax / 448.0f;
+    *qs = top / amax;
+    *ds = amax / top;
   }
 }
 
@@ -270,10 +294,12 @@ static void scale_of(float amax, float* qs, float* ds) {
 // (the emulator's per-tile scales that the "attention-numerics" page, method
 // and kernel settings, contrasts with the full-sequence API scales) and
 // descale[t] is tile t's; otherwise one scale for the slice.
-// Without `per_tile` the slice's amax is taken over its first P tokens.
+// Without `per_tile` the slice's amax is taken over its first P tokens.  With
+// `int8` the codes are symmetric INT8 (scale top 127, int8_encode) stored as
+// two's-complement bytes, otherwise E4M3 (top 448).
 static int prepare_slice(int N, int P, int d, int dtype, const void* X, bool rotate, const int8_t* signs,
                          const float* mu /* or null */, uint8_t* x8, float* descale, float* transformed_out,
-                         bool per_tile = false) {
+                         bool per_tile = false, bool int8 = false) {
   std::vector<float> t(size_t(N) * d);
   bool finite = true;
   for (int j = 0; j < N; ++j) {
@@ -297,9 +323,12 @@ static int prepare_slice(int N, int P, int d, int dtype, const void* X, bool rot
     float amax = 0.0f;
     for (size_t i = i0; i < a1; ++i) amax = std::max(amax, std::fabs(t[i]));
     float qs, ds;
-    scale_of(amax, &qs, &ds);
+    scale_of(amax, int8 ? 127.0f : 448.0f, &qs, &ds);
     descale[tile] = ds;
-    for (size_t i = i0; i < i1; ++i) x8[i] = e4m3_encode(t[i] * qs);
+    for (size_t i = i0; i < i1; ++i) {
+      const float y = t[i] * qs;
+      x8[i] = int8 ? uint8_t(int8_encode(y)) : e4m3_encode(y);
+    }
   }
   if (transformed_out) std::memcpy(transformed_out, t.data(), t.size() * sizeof(float));
   return ORC_OK;
@@ -312,6 +341,7 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
   if (stat_len < 0 || stat_len > N) return ORC_EINVAL;
   const int P = stat_len == 0 ? N : stat_len;  // tokens the mean and the slice scales see
   const bool rotate = flags & ORC_ROTATE, center = flags & ORC_CENTER_K, tiles = flags & ORC_TILE_SCALES;
+  const bool i8 = flags & ORC_I8QK;  // Q and K as INT8 codes, V stays E4M3
   if (rotate && !signs) return ORC_EINVAL;
   const size_t es = dtype == ORC_BF16 ? 2 : 4;
   const int64_t slice = int64_t(N) * d;
@@ -324,7 +354,7 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
     int rc;
     if (u < nq) {
       rc = prepare_slice(N, P, d, dtype, static_cast<const char*>(Q) + es * slice * u, rotate, signs, nullptr,
-                         q8 + slice * u, q_descale + per * u, nullptr, tiles);
+                         q8 + slice * u, q_descale + per * u, nullptr, tiles, i8);
     } else if (u < nq + nk) {
       int64_t g = u - nq;
       const void* Kh = static_cast<const char*>(K) + es * slice * g;
@@ -333,7 +363,8 @@ int orc_prepare(int B, int Hq, int Hkv, int N, int d, int dtype, unsigned flags,
         mu = &mus[size_t(g) * d];
         orc_mean_key(P, d, dtype, Kh, mu);  // the mean of the first P tokens
       }
-      rc = prepare_slice(N, P, d, dtype, Kh, rotate, signs, mu, k8 + slice * g, k_descale + per * g, nullptr, tiles);
+      rc = prepare_slice(N, P, d, dtype, Kh, rotate, signs, mu, k8 + slice * g, k_descale + per * g, nullptr, tiles,
+                         i8);
     } else {
       int64_t g = u - nq - nk;
       rc = prepare_slice(N, P, d, dtype, static_cast<const char*>(V) + es * slice * g, false, nullptr, nullptr,
@@ -482,7 +513,9 @@ void emulate_row(const RowCtx& x, int i, const double* qrow, KeyF key, ValF val,
 
 extern "C" {
 
-// Quantised forward on E4M3 operands in the natural [B, H, N, d] layout.
+// Quantised forward on E4M3 operands in the natural [B, H, N, d] layout (with
+// ORC_I8QK, q8 and k8 hold INT8 codes: q.k is then an exact integer sum, and
+// the descales are amax/127).
 // c = fl32(cq * dk) with cq = fl32(dq * (1/sqrt d) * (ROTATE ? 1/d : 1) * log2 e)
 // evaluated in double: the unnormalised FWHT on Q and K multiplies q.k by
 // exactly d.  Softmax scale reading: the pages do not state it; the standard
@@ -503,6 +536,7 @@ int orc_attn_quant(int B, int Hq, int Hkv, int N, int d, unsigned flags, const u
   const int group = Hq / Hkv;
   const int64_t slice = int64_t(N) * d;
   const bool rotate = flags & ORC_ROTATE;
+  const bool i8 = flags & ORC_I8QK;
   const int nst = tiles ? (N + ORC_SCALE_TILE - 1) / ORC_SCALE_TILE : 1;  // descales per Q/K slice
   const int RB = 16;
   const int64_t nblk = (n_rows + RB - 1) / RB;
@@ -531,10 +565,11 @@ int orc_attn_quant(int B, int Hq, int Hkv, int N, int d, unsigned flags, const u
         for (int t = 0; t < nst; ++t) c_tile[t] = logit_factor(qd[i / ORC_SCALE_TILE], kd[t]);
         x.c_tile = c_tile.data();
       }
-      for (int c = 0; c < d; ++c) q[c] = dec(qh[int64_t(i) * d + c]);
+      for (int c = 0; c < d; ++c) q[c] = i8 ? double(int8_t(qh[int64_t(i) * d + c])) : dec(qh[int64_t(i) * d + c]);
       float l;
       emulate_row(
-          x, i, q.data(), [&](int j, int c) { return dec(kh[int64_t(j) * d + c]); },
+          x, i, q.data(),
+          [&](int j, int c) { return i8 ? double(int8_t(kh[int64_t(j) * d + c])) : dec(kh[int64_t(j) * d + c]); },
           [&](int j, int c) { return dec(vh[int64_t(j) * d + c]); }, acc.data(), &l,
           underflow ? &uf_part[(size_t(ib) * nblk + rb) * 2] : nullptr);
       double* o = O + (int64_t(ib) * n_rows + r) * d;
