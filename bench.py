@@ -50,10 +50,12 @@ def attn_flops(B, Hq, N, d, rows=None):
     return 4.0 * d * pairs * B * Hq
 
 
-def prepare_bytes(B, Hq, Hkv, N, d, in_bytes=2):
-    """Algorithmic bytes of one prepare: read Q, K, V once, write their E4M3 codes once."""
+def prepare_bytes(B, Hq, Hkv, N, d, in_bytes=2, qk_code_bytes=1):
+    """Algorithmic bytes of one prepare: read Q, K, V once, write their codes once
+    (E4M3: 1 byte; INT8 Q/K codes held in bf16: 2 bytes)."""
     elems = (B * Hq + 2 * B * Hkv) * N * d
-    return elems * in_bytes + elems
+    qk = (B * Hq + B * Hkv) * N * d
+    return elems * in_bytes + (elems - qk) + qk * qk_code_bytes
 
 
 def load_peaks():
@@ -185,7 +187,7 @@ def dist_env():
 # oracle (CPU) sample: the CPU baseline and the reference arm
 # ---------------------------------------------------------------------------
 
-def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0, stat_len=0):
+def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0, stat_len=0, extra_flags=0):
     """Oracle prepare of one (batch, KV group) and quantised emulation of the
     given query rows of its query heads.  Returns (seconds, flops, threads)."""
     import oracle
@@ -195,8 +197,9 @@ def oracle_sample(q, k, v, signs, rows, heads_group=0, b=0, stat_len=0):
     vs = v[b:b + 1, heads_group:heads_group + 1]
     N, d = WL["N"], WL["d"]
     t0 = time.perf_counter()
-    prep = oracle.prepare(qs, ks, vs, flags=oracle.ROTATE | oracle.CENTER_K, signs=signs, stat_len=stat_len)
-    oracle.attn_quant(prep, (1, G, 1, N, d), oracle.ROTATE | oracle.CENTER_K, WL["S"], 1, True, WL["kv_tile"],
+    fl = oracle.ROTATE | oracle.CENTER_K | extra_flags
+    prep = oracle.prepare(qs, ks, vs, flags=fl, signs=signs, stat_len=stat_len)
+    oracle.attn_quant(prep, (1, G, 1, N, d), fl, WL["S"], 1, True, WL["kv_tile"],
                       rows=rows)
     dt = time.perf_counter() - t0
     return dt, attn_flops(1, G, N, d, rows=rows), oracle.threads()
@@ -339,6 +342,9 @@ def run_ours(args):
     flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT
     if args.scales == "tile":
         flags |= aq.ATTNQ_TILE_SCALES
+    i8 = args.qk == "int8"
+    if i8:
+        flags |= aq.ATTNQ_I8QK
     q_np, k_np, v_np = make_inputs(replica_seed(rank))
     signs_np = synth.hadamard_signs(17, d)
     dev = torch.device("cuda", local)
@@ -427,8 +433,11 @@ def run_ours(args):
     peaks = load_peaks()
     fp8_peak_sus = 2.0 * peaks["bf16_sus"]   # nominal fp8:bf16 dense ratio 4.5 : 2.25
     fp8_peak_burst = 2.0 * peaks["bf16"]
+    # INT8-QK: half the flops (Q K^T) on the bf16 path, half (P V) on fp8, so
+    # the step's tensor peak is 1 / (0.5 / bf16 + 0.5 / fp8) = 4/3 of bf16
+    mma_peak = 4.0 / 3.0 * peaks["bf16_sus"] if i8 else fp8_peak_sus
     fwd_tflops = flops_step / t_fwd / 1e12
-    prep_bytes = prepare_bytes(B, Hq, Hkv, N, d)
+    prep_bytes = prepare_bytes(B, Hq, Hkv, N, d, qk_code_bytes=2 if i8 else 1)
     prep_gbs = prep_bytes / t_prep / 1e9
     fwd_hash = kernel_source_hash(["attn_fwd.cu", "ptx.cuh"])
     prep_hash = kernel_source_hash(["prepare.cu", "ptx.cuh"])
@@ -447,7 +456,8 @@ def run_ours(args):
         cpu = None
         if not args.no_cpu_baseline:
             rows_s = sample_rows(args.cpu_rows)
-            dt, fl, thr = oracle_sample(q_np, k_np, v_np, signs_np, rows_s, stat_len=args.stat_len)
+            dt, fl, thr = oracle_sample(q_np, k_np, v_np, signs_np, rows_s, stat_len=args.stat_len,
+                                        extra_flags=oracle.I8QK if i8 else 0)
             cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                    "sample": (f"oracle prepare of one (batch, KV group) (4 query heads, 1 KV head) + quantised "
                               f"emulation of {len(rows_s)} query rows in [N/2, N) of those heads; "
@@ -455,18 +465,21 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8-qk/e4m3-pv" if i8 else "e4m3", "data": "synthetic",
             "config": {"workload": "long_context" if (B, Hq, Hkv) == (2, 32, 8) else "long_context_reduced", **WL, "rotate": True, "center_k": True, "scales": "per-tile (128 tokens)" if args.scales == "tile" else "per (batch, head)",
-                       "statistics": f"first {args.stat_len} tokens" if args.stat_len else "full sequence", "in_dtype": "bf16",
+                       "statistics": f"first {args.stat_len} tokens" if args.stat_len else "full sequence",
+                       "qk_codes": "int8 (held in bf16)" if i8 else "e4m3", "in_dtype": "bf16",
                        "out_dtype": "bf16", "step": "attnq_prepare + attnq_fwd",
                        "l2": "inputs 805 MB per step > 129 MB L2; no flush",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_fp8_peak": 100.0 * value / world / fp8_peak_sus,
             "roofline": {"kernel": "attnq_fwd (k_attn_fwd<128,128>)", "bound": "tensor", "achieved": fwd_tflops,
-                         "peak": fp8_peak_sus, "unit": "TFLOP/s", "frac": fwd_tflops / fp8_peak_sus,
+                         "peak": mma_peak, "unit": "TFLOP/s", "frac": fwd_tflops / mma_peak,
                          "traffic": ncu_traffic("k_attn_fwd", fwd_hash),
-                         "peak_note": (f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 2 (nominal fp8:bf16);"
-                                       f" burst-based peak {fp8_peak_burst:.1f}"),
+                         "peak_note": ((f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 4/3 (Q K^T on the bf16 "
+                                        f"path, P V on fp8 at 2 x bf16)") if i8 else
+                                       (f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 2 (nominal fp8:bf16);"
+                                        f" burst-based peak {fp8_peak_burst:.1f}")),
                          "flops_per_launch": flops_step, "ms_per_launch": t_fwd * 1e3},
             "roofline_prepare": {"kernel": "attnq_prepare (all passes)", "bound": "hbm", "achieved": prep_gbs,
                                  "peak": peaks["hbm"], "unit": "GB/s", "frac": prep_gbs / peaks["hbm"],
@@ -500,6 +513,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--scales", choices=["slice", "tile"], default="slice",
                     help="Q/K scales per (batch, head) (the timed workload) or per 128-token tile")
+    ap.add_argument("--qk", choices=["e4m3", "int8"], default="e4m3",
+                    help="Q/K code format: E4M3 (the timed workload) or INT8 (INT8-QK / FP8-PV)")
     ap.add_argument("--stat-len", type=int, default=0,
                     help="causal-prefix statistics: mean key and slice scales over the first P tokens (0: all N)")
     ap.add_argument("--B", type=int, default=WL["B"], help="smaller batch for profiling captures")

@@ -52,7 +52,7 @@ typedef enum {
 } attnq_status;
 
 /* desc.flags */
-enum { ATTNQ_ROTATE = 1u, ATTNQ_CENTER_K = 2u, ATTNQ_VT_LAYOUT = 4u, ATTNQ_TILE_SCALES = 8u };
+enum { ATTNQ_ROTATE = 1u, ATTNQ_CENTER_K = 2u, ATTNQ_VT_LAYOUT = 4u, ATTNQ_TILE_SCALES = 8u, ATTNQ_I8QK = 16u };
 /* tokens per scale tile of ATTNQ_TILE_SCALES */
 enum { ATTNQ_SCALE_TILE = 128 };
 /* element types of Q/K/V inputs and of O */
@@ -77,6 +77,16 @@ enum { ATTNQ_KV_FORWARD = 0, ATTNQ_KV_REVERSE = 1 };
  *                   the "attention-numerics" page, method and kernel settings,
  *                   contrasts with the API's full-sequence scales); V keeps
  *                   one scale per (batch, head).
+ *   ATTNQ_I8QK      INT8-QK / FP8-PV (the INT8-QK / FP8-PV kernel the
+ *                   "attention-numerics" page, method and kernel settings,
+ *                   runs; the page names only the formats): Q and K get
+ *                   symmetric INT8 codes, the nearest integer (ties to even)
+ *                   of fl32(x * qs) with qs = 127/amax, saturated to +-127,
+ *                   stored as bf16 values (2 bytes per code: the integers are
+ *                   exact in bf16, and GB300 multiplies them exactly on its
+ *                   bf16 tensor path, its INT8 path being far slower); q.k is
+ *                   then an exact integer sum (|q.k| <= 128 * 127^2 < 2^24, so
+ *                   fp32 accumulation keeps it exactly).  V and P stay E4M3.
  * signs: DEVICE pointer to d int8 values, each +1 or -1; required when
  * ATTNQ_ROTATE is set, ignored otherwise.
  * stat_len: 0 (full sequence), or P in 1..N: causal-prefix statistics.  The
@@ -148,12 +158,14 @@ size_t attnq_prepare_workspace(const attnq_desc* desc);
  *      butterfly stages h = 1, 2, ..., d/2;
  *   4. amax = max |x| over the first P tokens of the slice (over each
  *      128-token tile for Q and K with ATTNQ_TILE_SCALES); descale =
- *      amax/448 and qs = 448/amax (IEEE fp32 division; 1 and 1 when
- *      amax == 0);
- *   5. x8 = E4M3 code of fl32(x * qs), round-to-nearest-even, saturating.
+ *      amax/top and qs = top/amax (IEEE fp32 division; 1 and 1 when
+ *      amax == 0), top = 448, or 127 for Q and K with ATTNQ_I8QK;
+ *   5. x8 = E4M3 code of fl32(x * qs), round-to-nearest-even, saturating
+ *      (Q and K with ATTNQ_I8QK: the INT8 code of fl32(x * qs) as a bf16).
  * Q, K, V: DEVICE, in_dtype elements, [B,H,N,d].  q8 [B,Hq,N,d], k8
- * [B,Hkv,N,d]: DEVICE uint8 E4M3 codes.  v8: [B,Hkv,N,d], or
- * [B,Hkv,d,attnq_vt_ld(N)] with ATTNQ_VT_LAYOUT.  out: descales (and the
+ * [B,Hkv,N,d]: DEVICE uint8 E4M3 codes (with ATTNQ_I8QK: bf16, 2 bytes
+ * each).  v8: [B,Hkv,N,d], or [B,Hkv,d,attnq_vt_ld(N)] with
+ * ATTNQ_VT_LAYOUT.  out: descales (and the
  * optional mean key) as DEVICE pointers.  workspace: DEVICE, at least
  * attnq_prepare_workspace(desc) bytes, 256-byte aligned; its contents need no
  * initialisation and are garbage afterwards.  A non-finite value in an input
@@ -191,7 +203,8 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
  * the KV tiles of width kv_tile (aligned at token 0) holding a key j <= i
  * (every key when causal == 0), visited forward (0 -> diagonal) or reverse
  * (diagonal -> 0):
- *   s_j = q8_i . k8_j (exact products, fp32 accumulation);
+ *   s_j = q8_i . k8_j (exact products, fp32 accumulation; with ATTNQ_I8QK
+ *         an exact integer sum of INT8 codes held in bf16);
  *   t_j = s_j * c,  c = fl32(cq * dk), cq = fl32(dq / sqrt(d) * (ROTATE ? 1/d : 1) * log2 e)
  *   (cq in double);
  *   m' = max(m, max_j t_j);  alpha = 2^(m - m');  P_j = 2^(t_j - m');
@@ -257,7 +270,8 @@ attnq_status attnq_ref_attention(const attnq_desc* desc, const void* Q, const vo
  * against attnq_ref_attention to err_out[c * B*Hq + bh] (DEVICE fp64 [4][B*Hq]).
  * A head's rotation harm score is err[1] - err[0] (the pages average it over
  * the batch, their "texts").  desc->signs (DEVICE, d entries of +-1) is
- * required; desc->flags is ignored.  workspace: DEVICE, 256-byte aligned, at
+ * required; desc->flags is ignored (the conditions use E4M3 codes and one
+ * scale per (batch, head)); desc->stat_len applies.  workspace: DEVICE, 256-byte aligned, at
  * least attnq_harm_workspace(desc) bytes (it holds the fp64 reference, the
  * fp32 output, the E4M3 operands and the prepare workspace).  Errors of any
  * step are returned as that step returns them.

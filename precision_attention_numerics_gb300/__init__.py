@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     ATTNQ_ROTATE,
     ATTNQ_SCALE_TILE,
     ATTNQ_TILE_SCALES,
+    ATTNQ_I8QK,
     ATTNQ_VT_LAYOUT,
     AttnqDesc,
     AttnqError,

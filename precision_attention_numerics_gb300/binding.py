@@ -17,6 +17,7 @@ ATTNQ_ROTATE = 1
 ATTNQ_CENTER_K = 2
 ATTNQ_VT_LAYOUT = 4
 ATTNQ_TILE_SCALES = 8
+ATTNQ_I8QK = 16
 ATTNQ_SCALE_TILE = 128
 ATTNQ_F32 = 0
 ATTNQ_BF16 = 1

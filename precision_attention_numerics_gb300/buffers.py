@@ -3,7 +3,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-from .binding import (ATTNQ_TILE_SCALES, ATTNQ_VT_LAYOUT, AttnqDesc, AttnqScales, attnq_prepare_workspace,
+from .binding import (ATTNQ_I8QK, ATTNQ_TILE_SCALES, ATTNQ_VT_LAYOUT, AttnqDesc, AttnqScales, attnq_prepare_workspace,
                       attnq_scale_tiles, attnq_vt_ld)
 
 
@@ -17,11 +17,13 @@ class PreparedBuffers:
 
 
 def alloc_prepared(desc: AttnqDesc, device="cuda", with_mean: bool = True) -> PreparedBuffers:
-    """E4M3 operand tensors, descales, optional mean key and workspace for `desc`."""
+    """Operand tensors (E4M3 codes; Q and K as bf16-held INT8 codes with
+    ATTNQ_I8QK), descales, optional mean key and workspace for `desc`."""
     import torch
     B, Hq, Hkv, N, d = desc.B, desc.Hq, desc.Hkv, desc.N, desc.d
-    q8 = torch.empty((B, Hq, N, d), dtype=torch.uint8, device=device)
-    k8 = torch.empty((B, Hkv, N, d), dtype=torch.uint8, device=device)
+    qk_dtype = torch.bfloat16 if desc.flags & ATTNQ_I8QK else torch.uint8
+    q8 = torch.empty((B, Hq, N, d), dtype=qk_dtype, device=device)
+    k8 = torch.empty((B, Hkv, N, d), dtype=qk_dtype, device=device)
     if desc.flags & ATTNQ_VT_LAYOUT:
         v8 = torch.empty((B, Hkv, d, attnq_vt_ld(N)), dtype=torch.uint8, device=device)
     else:

@@ -57,7 +57,7 @@ attnq_status check_desc(const attnq_desc* d) {
   if (!d) return ATTNQ_EINVAL;
   if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0 || d->d <= 0) return ATTNQ_EINVAL;
   if (d->Hq % d->Hkv != 0) return ATTNQ_EINVAL;
-  if ((d->flags & ~uint32_t(ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT | ATTNQ_TILE_SCALES)) != 0)
+  if ((d->flags & ~uint32_t(ATTNQ_ROTATE | ATTNQ_CENTER_K | ATTNQ_VT_LAYOUT | ATTNQ_TILE_SCALES | ATTNQ_I8QK)) != 0)
     return ATTNQ_EINVAL;
   if (d->stat_len < 0 || d->stat_len > d->N) return ATTNQ_EINVAL;
   if (d->d != 64 && d->d != 128) return ATTNQ_EUNSUPPORTED;
@@ -135,8 +135,9 @@ PipeLayout pipe_layout(const attnq_desc* d, int32_t out_dtype) {
   for (int b = 0; b < 2; ++b)
     for (int t = 0; t < 3; ++t) L.in[b][t] = take(L.in_bytes[t]);
   const size_t nst = (d->flags & ATTNQ_TILE_SCALES) ? size_t(attnq_scale_tiles(d->N)) : 1;
-  L.q8 = take(nq * rows);
-  L.k8 = take(nk * rows);
+  const size_t qe = (d->flags & ATTNQ_I8QK) ? 2 : 1;  // bytes of a Q/K code
+  L.q8 = take(qe * nq * rows);
+  L.k8 = take(qe * nk * rows);
   L.v8 = take(nk * size_t(d->d) * size_t(attnq_vt_ld(d->N)));
   L.q_ds = take(4 * nq * nst);
   L.k_ds = take(4 * nk * nst);
@@ -216,6 +217,7 @@ PrepareArgs prepare_args(const attnq_desc* desc, const void* Q, const void* K, c
   a.center = (desc->flags & ATTNQ_CENTER_K) != 0;
   a.vt = (desc->flags & ATTNQ_VT_LAYOUT) != 0;
   a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
+  a.i8 = (desc->flags & ATTNQ_I8QK) != 0;
   a.signs = desc->signs;
   a.Q = Q; a.K = K; a.V = V; a.q8 = q8; a.k8 = k8; a.v8 = v8;
   a.q_ds = out->q_descale; a.k_ds = out->k_descale; a.v_ds = out->v_descale; a.k_mean = out->k_mean;
@@ -339,6 +341,7 @@ attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t*
   a.causal = causal; a.reverse = kv_order == ATTNQ_KV_REVERSE;
   a.rotate = (desc->flags & ATTNQ_ROTATE) != 0;
   a.tiles = (desc->flags & ATTNQ_TILE_SCALES) != 0;
+  a.i8 = (desc->flags & ATTNQ_I8QK) != 0;
   a.S = S;
   a.q8 = q8; a.k8 = k8; a.v8t = v8; a.ldv = attnq_vt_ld(desc->N);
   a.q_ds = scales->q_descale; a.k_ds = scales->k_descale; a.v_ds = scales->v_descale;

@@ -97,22 +97,34 @@ struct Params {
   uint64_t wait_ns;
 };
 
-template <int D, int T>
+// I8: Q and K hold INT8 codes as bf16 (2 bytes an element) and S = Q K^T runs
+// as kind::f16; P and V^T stay E4M3.
+template <int D, int T, bool I8 = false>
 struct Cfg {
-  static constexpr int QB = kRows * D;  // bytes of one Q tile
-  static constexpr int PB = kRows * T;  // bytes of one P tile
-  static constexpr int KB = T * D;      // bytes of one K stage
-  static constexpr int VB = D * T;      // bytes of one V^T stage
-  static constexpr int NS0 = (230400 - 4 * QB - 4 * PB) / (KB + VB);
+  static constexpr int QE = I8 ? 2 : 1;      // bytes of a Q/K element
+  static constexpr int QB = kRows * D * QE;  // bytes of one Q tile
+  static constexpr int PB = kRows * T;       // bytes of one P tile
+  static constexpr int KB = T * D * QE;      // bytes of one K stage
+  static constexpr int VB = D * T;           // bytes of one V^T stage
+  // Q buffers (units whose Q tiles are resident): two, so the next unit's Q
+  // loads during this one, unless that leaves fewer than two K/V stages
+  static constexpr int QBUF = (230400 - 4 * QB - 4 * PB) / (KB + VB) >= 2 ? 2 : 1;
+  static constexpr int NS0 = (230400 - 2 * QBUF * QB - 4 * PB) / (KB + VB);
   static constexpr int NS = NS0 > 6 ? 6 : NS0;
   static constexpr int COLS_USED = 2 * T + 2 * D;
   static constexpr uint32_t TMEM_COLS = COLS_USED <= 256 ? 256u : 512u;
-  static constexpr uint32_t LAYOUT_QK = D == 128 ? 2u : 4u;  // 128B / 64B swizzle
-  static constexpr uint32_t SBO_QK = 8u * D;
+  // Q/K rows are D * QE bytes: 128-byte swizzle atoms side by side along K
+  // (column blocks of rows x 128 bytes), or one 64-byte swizzled block for
+  // 64-byte rows
+  static constexpr uint32_t LAYOUT_QK = D * QE >= 128 ? 2u : 4u;  // 128B / 64B swizzle
+  static constexpr uint32_t SBO_QK = D * QE >= 128 ? 1024u : 512u;
+  static constexpr int QK_BLOCKS = D * QE >= 128 ? D * QE / 128 : 1;  // column blocks of a Q/K tile
+  static constexpr int QK_BOX = D * QE >= 128 ? 128 : D * QE;         // bytes of a TMA box row
   static constexpr uint32_t LAYOUT_V = T == 128 ? 2u : 4u;    // V^T and P rows are T bytes
   static constexpr uint32_t SBO_V = 8u * T;
   static constexpr int NBARS = 4 + 4 * NS + 14 + 2;
-  static constexpr size_t SMEM = 1024 + 4 * size_t(QB) + 4 * size_t(PB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
+  static constexpr size_t SMEM =
+      1024 + 2 * QBUF * size_t(QB) + 4 * size_t(PB) + size_t(NS) * (KB + VB) + 8 * NBARS + 16;
   static_assert(COLS_USED <= 512, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NS >= 2, "pipeline depth");
@@ -189,10 +201,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
-template <int D, int T>
+template <int D, int T, bool I8>
 __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                          uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
-  using C = Cfg<D, T>;
+  using C = Cfg<D, T, I8>;
   uint32_t it = 0, kc = 0, vc = 0;  // tiles walked, K and V loads issued
   int uc = 0;
   bool ok = true;
@@ -200,12 +212,18 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
   int q_last = 0;
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
     const Unit un = decode_unit<T>(p, u);
-    const int qb = uc & 1;
-    if (!wait_or_abort(br.q_empty + qb, ((uc >> 1) & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
+    const int qb = uc % C::QBUF;
+    if (!wait_or_abort(br.q_empty + qb, ((uc / C::QBUF) & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
     uint8_t* q_dst = sQ + size_t(qb) * 2 * C::QB;
     mbar_arrive_expect_tx(br.q_full + qb, un.nact * C::QB);
-    tma_load_3d(q_dst, tq, br.q_full + qb, 0, un.t * kRows, un.b * p.Hq + un.h0);
-    if (un.nact == 2) tma_load_3d(q_dst + C::QB, tq, br.q_full + qb, 0, un.t * kRows, un.b * p.Hq + un.h0 + 1);
+#pragma unroll
+    for (int cb = 0; cb < C::QK_BLOCKS; ++cb) {
+      tma_load_3d(q_dst + cb * (kRows * C::QK_BOX), tq, br.q_full + qb, cb * C::QK_BOX, un.t * kRows,
+                  un.b * p.Hq + un.h0);
+      if (un.nact == 2)
+        tma_load_3d(q_dst + C::QB + cb * (kRows * C::QK_BOX), tq, br.q_full + qb, cb * C::QK_BOX, un.t * kRows,
+                    un.b * p.Hq + un.h0 + 1);
+    }
     q_issued = true;
     q_last = uc;
     const int zkv = un.b * p.Hkv + un.g;
@@ -215,7 +233,9 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
       const uint32_t ph = (it / C::NS) & 1u;
       if (!wait_or_abort(br.k_empty + s, ph ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(br.k_full + s, C::KB);
-      tma_load_3d(sK + size_t(s) * C::KB, tk, br.k_full + s, 0, jt * T, zkv);
+#pragma unroll
+      for (int cb = 0; cb < C::QK_BLOCKS; ++cb)
+        tma_load_3d(sK + size_t(s) * C::KB + cb * (T * C::QK_BOX), tk, br.k_full + s, cb * C::QK_BOX, jt * T, zkv);
       ++kc;
       if (!wait_or_abort(br.v_empty + s, ph ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(br.v_full + s, C::VB);
@@ -230,9 +250,9 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
     const uint64_t limit = kDrainNs;
     volatile int no_abort = 0;
     if (q_issued) {
-      // the last two Q loads may still be in flight
-      for (int x = q_last; x >= 0 && x >= q_last - 1; --x)
-        wait_or_abort(br.q_full + (x & 1), (x >> 1) & 1, limit, &no_abort);
+      // the last QBUF Q loads may still be in flight
+      for (int x = q_last; x >= 0 && x > q_last - C::QBUF; --x)
+        wait_or_abort(br.q_full + (x % C::QBUF), (x / C::QBUF) & 1, limit, &no_abort);
     }
     for (uint32_t x = 0; x < uint32_t(C::NS); ++x) {
       if (x < kc) {
@@ -273,11 +293,11 @@ struct Ring {
 // K/V stage and Q buffer barriers take one arrival from each of the two
 // issuing warps (a commit when the warp's warpgroup used them, a plain arrive
 // when it sat the unit out).
-template <int D, int T>
+template <int D, int T, bool I8>
 __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem, uint8_t* sQ, uint8_t* sP,
                                            uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
-  using C = Cfg<D, T>;
-  constexpr uint32_t idS = idesc_e4m3_f32(kRows, T);
+  using C = Cfg<D, T, I8>;
+  constexpr uint32_t idS = I8 ? idesc_bf16_f32(kRows, T) : idesc_e4m3_f32(kRows, T);
   constexpr uint32_t idO = idesc_e4m3_f32(kRows, D);
   // descriptor = {start address field (low word), constant high word}
   const uint32_t hQK = uint32_t(smem_desc(0, 16, C::SBO_QK, C::LAYOUT_QK) >> 32);
@@ -303,9 +323,20 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
     ++n_s;
     tc_fence_after();
     const uint32_t lk = lK0 + rk.s * uint32_t(C::KB >> 4);
+    if constexpr (I8) {
+      // K steps of 16 bf16 (32 bytes): four per 128-byte column block, then
+      // the next block (rows x 128 bytes further on)
 #pragma unroll
-    for (int kk = 0; kk < D / 32; ++kk)
-      mma_f8_ss_elect(tS, pack_desc(lq + 2 * kk, hQK), pack_desc(lk + 2 * kk, hQK), idS, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t cb = uint32_t(kk >> 2), sub = uint32_t(2 * (kk & 3));
+        mma_f16_ss_elect(tS, pack_desc(lq + cb * uint32_t(kRows * 8) + sub, hQK),
+                         pack_desc(lk + cb * uint32_t(T * 8) + sub, hQK), idS, kk > 0 ? 1u : 0u);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < D / 32; ++kk)
+        mma_f8_ss_elect(tS, pack_desc(lq + 2 * kk, hQK), pack_desc(lk + 2 * kk, hQK), idS, kk > 0 ? 1u : 0u);
+    }
     mma_commit_elect(br.s_full + w);
     mma_commit_elect(br.k_empty + rk.s);
     rk.next(C::NS);
@@ -315,8 +346,8 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
 
   for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
     const Unit un = decode_unit<T>(p, u);
-    const int qb = uc & 1;
-    if (!vote_wait(br.q_full + qb, (uc >> 1) & 1, p, abort_flag)) { ok = false; break; }
+    const int qb = uc % C::QBUF;
+    if (!vote_wait(br.q_full + qb, (uc / C::QBUF) & 1, p, abort_flag)) { ok = false; break; }
     tc_fence_after();
     if (w >= un.nact) {
       // this warpgroup sits the unit out: release each stage and the Q buffer
@@ -617,18 +648,18 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
   if (!ok) raise_abort(p, abort_flag);
 }
 
-template <int D, int T, bool COUNT, bool TILES>
+template <int D, int T, bool COUNT, bool TILES, bool I8>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const Params p) {
-  using C = Cfg<D, T>;
+  using C = Cfg<D, T, I8>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base by pointer arithmetic on the shared array (an
   // integer round trip would hide the address space and make every access
   // through it a generic one)
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = sm;                      // [Q buffer][warpgroup]
-  uint8_t* sP = sQ + 4 * C::QB;          // [warpgroup][P buffer]
+  uint8_t* sQ = sm;                          // [Q buffer][warpgroup]
+  uint8_t* sP = sQ + 2 * C::QBUF * C::QB;    // [warpgroup][P buffer]
   uint8_t* sK = sP + 4 * C::PB;
   uint8_t* sV = sK + size_t(C::NS) * C::KB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + size_t(C::NS) * C::VB);
@@ -690,9 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= 8) {
     regs_decrease<kControlRegs>();
     if (warp == kProducerWarp) {
-      if (lane == 0) producer<D, T>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
+      if (lane == 0) producer<D, T, I8>(p, &tq, &tk, &tv, sQ, sK, sV, br, abort_flag);
     } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-      mma_issuer<D, T>(p, warp - kMmaWarp, tmem, sQ, sP, sK, sV, br, abort_flag);
+      mma_issuer<D, T, I8>(p, warp - kMmaWarp, tmem, sQ, sP, sK, sV, br, abort_flag);
     }
   } else {
     regs_increase<kSoftmaxRegs>();
@@ -707,15 +738,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int T, bool COUNT, bool TILES>
+template <int D, int T, bool COUNT, bool TILES, bool I8>
 cudaError_t run(const FwdArgs& a, cudaStream_t st) {
-  using C = Cfg<D, T>;
+  using C = Cfg<D, T, I8>;
   CUtensorMap tq, tk, tv;
-  const CUtensorMapSwizzle swqk = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUtensorMapSwizzle swqk = C::LAYOUT_QK == 2u ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   const CUtensorMapSwizzle swv = T == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if (encode_tiled_3d(&tq, a.q8, D, a.N, uint64_t(a.B) * a.Hq, D, uint64_t(a.N) * D, D, kRows, swqk) != CUDA_SUCCESS)
+  const uint64_t rq = uint64_t(D) * C::QE;  // bytes of a Q/K row
+  if (encode_tiled_3d(&tq, a.q8, rq, a.N, uint64_t(a.B) * a.Hq, rq, uint64_t(a.N) * rq, C::QK_BOX, kRows, swqk) !=
+      CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  if (encode_tiled_3d(&tk, a.k8, D, a.N, uint64_t(a.B) * a.Hkv, D, uint64_t(a.N) * D, D, T, swqk) != CUDA_SUCCESS)
+  if (encode_tiled_3d(&tk, a.k8, rq, a.N, uint64_t(a.B) * a.Hkv, rq, uint64_t(a.N) * rq, C::QK_BOX, T, swqk) !=
+      CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   if (encode_tiled_3d(&tv, a.v8t, uint64_t(a.ldv), D, uint64_t(a.B) * a.Hkv, uint64_t(a.ldv), uint64_t(a.ldv) * D, T,
                       D, swv) != CUDA_SUCCESS)
@@ -747,7 +781,7 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   p.k_sink = a.k_sink;
   p.status = a.status;
   p.wait_ns = a.wait_ns;
-  auto kern = k_attn_fwd<D, T, COUNT, TILES>;
+  auto kern = k_attn_fwd<D, T, COUNT, TILES, I8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
@@ -755,17 +789,22 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, int T>
+template <int D, int T, bool I8>
 cudaError_t run_count(const FwdArgs& a, cudaStream_t st) {
-  if (a.tiles) return a.underflow ? run<D, T, true, true>(a, st) : run<D, T, false, true>(a, st);
-  return a.underflow ? run<D, T, true, false>(a, st) : run<D, T, false, false>(a, st);
+  if (a.tiles) return a.underflow ? run<D, T, true, true, I8>(a, st) : run<D, T, false, true, I8>(a, st);
+  return a.underflow ? run<D, T, true, false, I8>(a, st) : run<D, T, false, false, I8>(a, st);
+}
+
+template <int D, int T>
+cudaError_t run_format(const FwdArgs& a, cudaStream_t st) {
+  return a.i8 ? run_count<D, T, true>(a, st) : run_count<D, T, false>(a, st);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t s) {
-  if (a.d == 128) return a.T == 128 ? run_count<128, 128>(a, s) : run_count<128, 64>(a, s);
-  return a.T == 128 ? run_count<64, 128>(a, s) : run_count<64, 64>(a, s);
+  if (a.d == 128) return a.T == 128 ? run_format<128, 128>(a, s) : run_format<128, 64>(a, s);
+  return a.T == 128 ? run_format<64, 128>(a, s) : run_format<64, 64>(a, s);
 }
 
 }  // namespace attnq

@@ -18,6 +18,7 @@ struct PrepareArgs {
   int bf16;           // input element type: 1 bf16, 0 fp32
   int rotate, center, vt;
   int tiles;          // per-tile Q/K scales
+  int i8;             // Q and K as INT8 codes held in bf16 (V stays E4M3)
   const int8_t* signs;
   const void* Q;
   const void* K;
@@ -58,6 +59,7 @@ struct FwdArgs {
   int causal, reverse;
   int rotate;
   int tiles;          // per-tile Q/K scales
+  int i8;             // q8, k8: INT8 codes held in bf16 (S = Q K^T as kind::f16)
   float S;
   const uint8_t* q8;
   const uint8_t* k8;

@@ -70,14 +70,18 @@ constexpr int kLagA = 4, kLagC = 7;  // least list steps from a K slice's M entr
 constexpr uint32_t KIND_M = 0u, KIND_A = 1u, KIND_C = 2u, KIND_DONE = 3u;
 constexpr uint32_t CTL_TICKET = 0, CTL_ABORT = 1, CTL_ENTRIES = 2;
 
-template <int D, bool BF16>
+// I8: Q and K leave as INT8 codes held in bf16 (2 bytes a code), so a warp's
+// staging buffer is twice as large and each warp keeps one of them.
+template <int D, bool BF16, bool I8 = false>
 struct FlowCfg {
   static constexpr int ES = BF16 ? 2 : 4;
   static constexpr int ROW_BYTES = D * ES;
   static constexpr int NB = ROW_BYTES / 128;      // 128-byte boxes per input row
   static constexpr int SB = kTR * ROW_BYTES;      // input stage
-  static constexpr int WB = 32 * D;               // a consumer warp's staging buffer (32 rows of codes)
-  static constexpr int NST0 = (225280 - 2 * kConsumerWarps * WB - 8192) / SB;
+  static constexpr int WB = (I8 ? 64 : 32) * D;   // a consumer warp's staging buffer (32 rows of codes)
+  static constexpr int NBUF = I8 ? 1 : 2;         // staging buffers per consumer warp
+  static constexpr int NOB = I8 ? (2 * D) / 128 : 1;  // 128-byte boxes per row of bf16 codes
+  static constexpr int NST0 = (225280 - NBUF * kConsumerWarps * WB - 8192) / SB;
   // A multiple of kGroups: tile n goes to stage n % NST and to group
   // n % kGroups, so every stage serves one group only and its phases are
   // consumed in order.  A stage shared by two groups would let a group whose
@@ -85,7 +89,7 @@ struct FlowCfg {
   static constexpr int NST1 = NST0 > 6 ? 6 : NST0;
   static constexpr int NST = NST1 - NST1 % kGroups;
   static constexpr int WORDS = BF16 ? D / 2 : D;  // 32-bit input words per row
-  static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(2 * kConsumerWarps) * WB + 16 * NST +
+  static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(NBUF * kConsumerWarps) * WB + 16 * NST +
                                  16 * NST + 4 * WORDS + 8 * (D / 2) + kConsumerWarps * 8 * (D / 2) +
                                  4 * 4 * 2 * kGroups + 8 * 2 * kGroups;
   static_assert(NST >= kGroups && NST % kGroups == 0, "pipeline depth: whole stages per group");
@@ -262,9 +266,10 @@ __device__ __forceinline__ void flag_set(uint32_t* flag) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(1u) : "memory");
 }
 
-// qs = 448/amax, descale = amax/448 (IEEE division); amax = 0 -> 1, 1; a NaN
-// or an infinity in the slice gives qs = 0 and a NaN descale.
-__device__ __forceinline__ void scale_from_amax(uint32_t bits, float& qs, float& ds) {
+// qs = top/amax, descale = amax/top (IEEE division; top = 448 for E4M3 codes,
+// 127 for INT8 codes); amax = 0 -> 1, 1; a NaN or an infinity in the slice
+// gives qs = 0 and a NaN descale.
+__device__ __forceinline__ void scale_from_amax(uint32_t bits, float top, float& qs, float& ds) {
   if (bits >= 0x7F800000u) {
     qs = 0.0f;
     ds = __uint_as_float(0x7FC00000u);
@@ -273,8 +278,8 @@ __device__ __forceinline__ void scale_from_amax(uint32_t bits, float& qs, float&
     ds = 1.0f;
   } else {
     const float amax = __uint_as_float(bits);
-    qs = __fdiv_rn(448.0f, amax);
-    ds = __fdiv_rn(amax, 448.0f);
+    qs = __fdiv_rn(top, amax);
+    ds = __fdiv_rn(amax, top);
   }
 }
 
@@ -290,10 +295,10 @@ __device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
 
 // ---- producer -------------------------------------------------------------
 // PREFIX: statistics over the first P < N tokens (the M and A entries stop there).
-template <int D, bool BF16, bool PREFIX>
+template <int D, bool BF16, bool PREFIX, bool I8>
 __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8_t* stages, TileMeta* meta,
                          uint64_t* full, uint64_t* empty) {
-  using C = FlowCfg<D, BF16>;
+  using C = FlowCfg<D, BF16, I8>;
   const PrepareArgs& a = f.a;
   const uint32_t total = a.ctl[CTL_ENTRIES] * uint32_t(f.items_per_slice);
   // A slice's data is read again by a later pass (A after M, C after A):
@@ -553,6 +558,38 @@ __device__ __forceinline__ void row_codes(const uint64_t (&P)[D / 2], float qs, 
   }
 }
 
+// INT8 codes of a row held as pairs (x_j, x_{j+D/2}): the nearest integer of
+// fl32(x * qs), ties to even, saturated to +-127, as bf16 values (exact), into
+// the warp's staging buffer: boxes of 32 rows x 128 bytes (64 codes) in the
+// 128-byte swizzle, row = lane.  The product is rounded to an integer by one
+// round-to-integer instruction on the stored fp32 product.  (Adding and
+// subtracting 1.5 * 2^23 instead gave codes one too small where fl32(x * qs)
+// is an exact tie but the unrounded product lies just below it: the multiply
+// and the add were not rounded separately.)
+template <int D>
+__device__ __forceinline__ void row_int8_codes(const uint64_t (&P)[D / 2], float qs, uint8_t* ob, int lane) {
+  const uint64_t q2 = pack2(qs, qs);
+  const uint32_t lim_lo = 0xC2FEC2FEu, lim_hi = 0x42FE42FEu;  // -127, 127 in bf16
+#pragma unroll
+  for (int c8 = 0; c8 < D / 16; ++c8) {
+    // pairs 8 c8 .. 8 c8 + 7: codes 8 c8 .. (chunk c8) and D/2 + 8 c8 .. (chunk D/16 + c8)
+    uint32_t wl[4], wh[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a0, b0, a1, b1;
+      unpack2(fmul2(P[8 * c8 + 2 * i], q2), a0, b0);
+      unpack2(fmul2(P[8 * c8 + 2 * i + 1], q2), a1, b1);
+      wl[i] = bf16x2_clamp(rintf(a0), rintf(a1), lim_lo, lim_hi);
+      wh[i] = bf16x2_clamp(rintf(b0), rintf(b1), lim_lo, lim_hi);
+    }
+    const int ch = D / 16 + c8;
+    *reinterpret_cast<uint4*>(ob + (c8 >> 3) * 4096 + lane * 128 + (((c8 & 7) ^ (lane & 7)) << 4)) =
+        make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    *reinterpret_cast<uint4*>(ob + (ch >> 3) * 4096 + lane * 128 + (((ch & 7) ^ (lane & 7)) << 4)) =
+        make_uint4(wh[0], wh[1], wh[2], wh[3]);
+  }
+}
+
 // Mean key of K slice `sl` from the chunk sums of its first P tokens: per
 // channel, the `chunks` sums added in chunk order, then one division by P.
 // Lane l owns channels l, l + 32, ...; the loads run eight chunks ahead of the
@@ -589,14 +626,15 @@ __device__ __forceinline__ void finish_mean(const PrepareArgs& a, int tiles_per_
 
 // ---- the persistent kernel ----------------------------------------------------
 // PREFIX is the causal-prefix form (P < N); without it the kernel is the
-// full-sequence one and carries no prefix code.
-template <int D, bool BF16, bool PREFIX>
+// full-sequence one and carries no prefix code.  I8: Q and K get INT8 codes
+// (scale 127/amax) stored as bf16 values; V keeps E4M3.
+template <int D, bool BF16, bool PREFIX, bool I8>
 __global__ void __launch_bounds__(kFlowThreads, 1)
     k_prepare(const __grid_constant__ CUtensorMap in_q, const __grid_constant__ CUtensorMap in_k,
               const __grid_constant__ CUtensorMap in_v, const __grid_constant__ CUtensorMap out_q,
               const __grid_constant__ CUtensorMap out_k, const __grid_constant__ CUtensorMap out_v,
               const Flow f) {
-  using C = FlowCfg<D, BF16>;
+  using C = FlowCfg<D, BF16, I8>;
   const PrepareArgs& a = f.a;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base by pointer arithmetic on the shared array (an
@@ -605,7 +643,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stages = sm;
   uint8_t* outb = stages + size_t(C::NST) * C::SB;               // [consumer warp][2] staging buffers
-  TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(2 * kConsumerWarps) * C::WB);
+  TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(C::NBUF * kConsumerWarps) * C::WB);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + C::NST);
   uint64_t* empty = full + C::NST;
   uint32_t* smask = reinterpret_cast<uint32_t*>(empty + C::NST);  // sign-bit mask per input word
@@ -650,7 +688,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       tma_prefetch_desc(&in_k);
       tma_prefetch_desc(&in_v);
       const CUtensorMap* maps[3] = {&in_q, &in_k, &in_v};
-      producer<D, BF16, PREFIX>(f, maps, stages, meta, full, empty);
+      producer<D, BF16, PREFIX, I8>(f, maps, stages, meta, full, empty);
     }
     return;
   }
@@ -662,7 +700,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   regs_increase<kConsumerRegs>();
   const int g = warp >> 2, w4 = warp & 3, r = threadIdx.x & 127;
   uint64_t* nmu = nmu_all + warp * (D / 2);
-  uint8_t* obuf = outb + size_t(2 * warp) * C::WB;
+  uint8_t* obuf = outb + size_t(C::NBUF * warp) * C::WB;
   const uint32_t tiles = uint32_t(f.tiles_per_slice);
   const uint32_t stat_tiles = uint32_t(f.tiles_stat);  // M and A tiles of a slice
   const int plen = PREFIX ? a.P : a.N;                 // tokens the M and A passes cover
@@ -689,6 +727,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
     // rows the pass covers: every token for the cast, the first P for M and A
     const bool valid = row0 + r < (PREFIX && tm.kind != KIND_C ? plen : a.N);
     const bool qk = sr.tensor < 2;
+    const float top = (I8 && qk) ? 127.0f : 448.0f;  // largest code of the slice's format
     const bool rotate = a.rotate && qk, center = a.center && sr.tensor == 1;
 
     if (tm.kind == KIND_M) {
@@ -797,7 +836,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       ++xc;
       const uint32_t bits = max(max(tmax[4 * xb], tmax[4 * xb + 1]), max(tmax[4 * xb + 2], tmax[4 * xb + 3]));
       float ds;
-      scale_from_amax(bits, qs, ds);
+      scale_from_amax(bits, top, qs, ds);
       qs_slice = -1;  // qs is this tile's
       if (w4 == 0 && lane == 0) {
         (sr.tensor == 0 ? a.q_ds : a.k_ds)[int64_t(sr.local) * tiles + uint32_t(row0 / kScaleTile)] = ds;
@@ -809,13 +848,13 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
         if (!warp_count_wait(a, a.a_done + s, stat_tiles * 4u)) { ok = false; break; }
         qs_bits = __ldcg(a.amax_bits + s);
         float ds;
-        scale_from_amax(qs_bits, qs, ds);
+        scale_from_amax(qs_bits, top, qs, ds);
         qs_slice = s;
       }
       if (row0 == 0 && w4 == 0 && lane == 0) {
         // the warp with the slice's first rows publishes its descale
         float q2, ds;
-        scale_from_amax(qs_bits, q2, ds);
+        scale_from_amax(qs_bits, top, q2, ds);
         (sr.tensor == 0 ? a.q_ds : sr.tensor == 1 ? a.k_ds : a.v_ds)[sr.local] = ds;
         if (qs_bits >= 0x7F800000u) atomicOr(a.status, DEV_NONFINITE);
       }
@@ -827,40 +866,52 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       }
     }
     if (rotate) final_stage<D>(P);
-    uint32_t cw[D / 4];
-    row_codes<D>(P, qs, cw);
     const bool vt = sr.tensor == 2 && a.vt;
+    const bool i8row = I8 && qk;  // INT8 codes in bf16, two bytes a code
     const int x0 = row0 + 32 * w4;  // the warp's first row (token)
     if (int64_t(x0) >= (vt ? a.ldv : int64_t(a.N))) continue;  // all of the warp's rows are past the end
-    // the store that last read this buffer (two casts ago) must be done with it
-    if (stored && lane == 0) bulk_wait_read<1>();
+    // the store that last read this buffer (two casts ago; the last one with
+    // a single buffer) must be done with it
+    if (stored && lane == 0) bulk_wait_read<C::NBUF - 1>();
     __syncwarp();
-    uint8_t* ob = obuf + size_t(cbuf) * C::WB;
-    if (vt) {
-      // channel-major [D][32 tokens]: a 4 x 4 byte transpose within each quad
-      // of lanes turns word k of lane 4q + i (channels 4k .. 4k + 3 of token
-      // 4q + i) into channel 4k + i of tokens 4q .. 4q + 3, one 32-bit store
-      const int i4 = lane & 3;
-#pragma unroll
-      for (int k = 0; k < D / 4; ++k) {
-        const uint32_t w = cw[k];
-        // 16-bit halves with lane ^ 2, then bytes with lane ^ 1
-        const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w, 2);
-        const uint32_t w1 = (i4 & 2) ? __byte_perm(w, o1, 0x3276) : __byte_perm(w, o1, 0x5410);
-        const uint32_t o2 = __shfl_xor_sync(0xffffffffu, w1, 1);
-        const uint32_t w2 = (i4 & 1) ? __byte_perm(w1, o2, 0x3715) : __byte_perm(w1, o2, 0x6240);
-        *reinterpret_cast<uint32_t*>(ob + (4 * k + i4) * 32 + (lane & ~3)) = w2;
-      }
+    uint8_t* ob = obuf + size_t(C::NBUF > 1 ? cbuf : 0u) * C::WB;
+    if (i8row) {
+      row_int8_codes<D>(P, qs, ob, lane);
     } else {
+      uint32_t cw[D / 4];
+      row_codes<D>(P, qs, cw);
+      if (vt) {
+        // channel-major [D][32 tokens]: a 4 x 4 byte transpose within each quad
+        // of lanes turns word k of lane 4q + i (channels 4k .. 4k + 3 of token
+        // 4q + i) into channel 4k + i of tokens 4q .. 4q + 3, one 32-bit store
+        const int i4 = lane & 3;
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c)
-        *reinterpret_cast<uint4*>(ob + stage_off<D>(lane, c)) = make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+        for (int k = 0; k < D / 4; ++k) {
+          const uint32_t w = cw[k];
+          // 16-bit halves with lane ^ 2, then bytes with lane ^ 1
+          const uint32_t o1 = __shfl_xor_sync(0xffffffffu, w, 2);
+          const uint32_t w1 = (i4 & 2) ? __byte_perm(w, o1, 0x3276) : __byte_perm(w, o1, 0x5410);
+          const uint32_t o2 = __shfl_xor_sync(0xffffffffu, w1, 1);
+          const uint32_t w2 = (i4 & 1) ? __byte_perm(w1, o2, 0x3715) : __byte_perm(w1, o2, 0x6240);
+          *reinterpret_cast<uint32_t*>(ob + (4 * k + i4) * 32 + (lane & ~3)) = w2;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c)
+          *reinterpret_cast<uint4*>(ob + stage_off<D>(lane, c)) =
+              make_uint4(cw[4 * c], cw[4 * c + 1], cw[4 * c + 2], cw[4 * c + 3]);
+      }
     }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
       const uint64_t once = l2_evict_first_policy();  // codes are written once and read by a later kernel
-      if (vt) {
+      if (i8row) {
+        // one 128-byte box of 64 codes per store
+#pragma unroll
+        for (int b = 0; b < C::NOB; ++b)
+          tma_store_3d_hint(sr.tensor == 0 ? &out_q : &out_k, ob + b * 4096, b * 128, x0, sr.local, once);
+      } else if (vt) {
         tma_store_3d_hint(&out_v, ob, x0, 0, sr.local, once);
       } else {
         tma_store_3d_hint(sr.tensor == 0 ? &out_q : sr.tensor == 1 ? &out_k : &out_v, ob, 0, x0, sr.local, once);
@@ -887,10 +938,17 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
       encode_tiled_3d(&in_k, a.K, rb, N, nk, rb, rb * N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
       encode_tiled_3d(&in_v, a.V, rb, N, nk, rb, rb * N, 128, kTR, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  // outputs: 32-row boxes, one per consumer warp
-  if (encode_tiled_3d(&out_q, a.q8, D, N, nq, D, D * N, D, 32, swo) != CUDA_SUCCESS ||
-      encode_tiled_3d(&out_k, a.k8, D, N, nk, D, D * N, D, 32, swo) != CUDA_SUCCESS)
+  // outputs: 32-row boxes, one per consumer warp; INT8 Q/K codes are bf16
+  // rows of 2D bytes, stored as 128-byte boxes
+  if (a.i8) {
+    const uint64_t ob = 2 * uint64_t(D);
+    if (encode_tiled_3d(&out_q, a.q8, ob, N, nq, ob, ob * N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tiled_3d(&out_k, a.k8, ob, N, nk, ob, ob * N, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  } else if (encode_tiled_3d(&out_q, a.q8, D, N, nq, D, D * N, D, 32, swo) != CUDA_SUCCESS ||
+             encode_tiled_3d(&out_k, a.k8, D, N, nk, D, D * N, D, 32, swo) != CUDA_SUCCESS) {
     return cudaErrorInvalidValue;
+  }
   if (a.vt) {
     if (encode_tiled_3d(&out_v, a.v8, uint64_t(a.ldv), D, nk, uint64_t(a.ldv), uint64_t(a.ldv) * D, 32, D,
                         CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
@@ -904,11 +962,14 @@ cudaError_t run(const PrepareArgs& a, cudaStream_t st) {
   f.items_per_slice = (f.tiles_per_slice + kTilesPerItem - 1) / kTilesPerItem;
   f.tiles_stat = (a.P + kTR - 1) / kTR;
   k_flow_init<<<1, 256, 0, st>>>(a);
-  auto kern = a.P < a.N ? k_prepare<D, BF16, true> : k_prepare<D, BF16, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+  const bool prefix = a.P < a.N;
+  auto kern = a.i8 ? (prefix ? k_prepare<D, BF16, true, true> : k_prepare<D, BF16, false, true>)
+                   : (prefix ? k_prepare<D, BF16, true, false> : k_prepare<D, BF16, false, false>);
+  const size_t smem = a.i8 ? FlowCfg<D, BF16, true>::SMEM : C::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   const int grid = a.num_sms > 0 ? a.num_sms : 1;
-  kern<<<grid, kFlowThreads, C::SMEM, st>>>(in_q, in_k, in_v, out_q, out_k, out_v, f);
+  kern<<<grid, kFlowThreads, smem, st>>>(in_q, in_k, in_v, out_q, out_k, out_v, f);
   return cudaGetLastError();
 }
 

@@ -198,6 +198,16 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor for kind::f16 with bf16 A and B, fp32 D, both
+// operands K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)              // D format: f32
+         | (1u << 7)            // A: bf16
+         | (1u << 10)           // B: bf16
+         | ((N >> 3) << 17)     // N / 8
+         | ((M >> 4) << 24);    // M / 16
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T
 __device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
@@ -239,6 +249,17 @@ __device__ __forceinline__ void mma_f8_ss_elect(uint32_t d_tmem, uint64_t a_desc
       "elect.sync _|P, 0xffffffff;\n\t"
       "setp.ne.b32 A, %4, 0;\n\t"
       "@P tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, A;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// kind::f16 (bf16 A and B, fp32 accumulate) form of mma_f8_ss_elect.
+__device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, A;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "setp.ne.b32 A, %4, 0;\n\t"
+      "@P tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, A;\n\t}"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -371,6 +392,15 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
+}
+// Two floats to bf16 (round to nearest even; `lo` in the low half), then each
+// clamped to [lim_lo, lim_hi] given as bf16x2 pairs.
+__device__ __forceinline__ uint32_t bf16x2_clamp(float lo, float hi, uint32_t lim_lo2, uint32_t lim_hi2) {
+  uint32_t w;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
+  asm("max.bf16x2 %0, %0, %1;" : "+r"(w) : "r"(lim_lo2));
+  asm("min.bf16x2 %0, %0, %1;" : "+r"(w) : "r"(lim_hi2));
+  return w;
 }
 __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   uint64_t d;

@@ -39,7 +39,12 @@ def gpu_prepare(q, k, v, flags: int, signs=None, vt: bool = True, stat_len: int 
 def prepared_to_numpy(desc, bufs):
     """Device results in the oracle's layout (v8 untransposed)."""
     N = desc.N
-    out = dict(q8=bufs.q8.cpu().numpy(), k8=bufs.k8.cpu().numpy(),
+
+    def codes(t):
+        # INT8 codes held in bf16 come back as int8 (the values are exact integers)
+        return t.float().cpu().numpy().astype(np.int8) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+    out = dict(q8=codes(bufs.q8), k8=codes(bufs.k8),
                q_descale=bufs.scales.q_descale.cpu().numpy(), k_descale=bufs.scales.k_descale.cpu().numpy(),
                v_descale=bufs.scales.v_descale.cpu().numpy(),
                k_mean=bufs.scales.k_mean.cpu().numpy() if bufs.scales.k_mean is not None else None)
