@@ -440,6 +440,8 @@ def run_ours(args):
     prep_bytes = prepare_bytes(B, Hq, Hkv, N, d, qk_code_bytes=2 if i8 else 1)
     prep_gbs = prep_bytes / t_prep / 1e9
     fwd_hash = kernel_source_hash(["attn_fwd.cu", "ptx.cuh"])
+    # traffic is recorded per kernel and per workload variant
+    tag = ("_i8" if i8 else "") + ("_tile" if args.scales == "tile" else "") + (f"_p{args.stat_len}" if args.stat_len else "")
     prep_hash = kernel_source_hash(["prepare.cu", "ptx.cuh"])
 
     line = None
@@ -475,7 +477,7 @@ def run_ours(args):
             "pct_fp8_peak": 100.0 * value / world / fp8_peak_sus,
             "roofline": {"kernel": "attnq_fwd (k_attn_fwd<128,128>)", "bound": "tensor", "achieved": fwd_tflops,
                          "peak": mma_peak, "unit": "TFLOP/s", "frac": fwd_tflops / mma_peak,
-                         "traffic": ncu_traffic("k_attn_fwd", fwd_hash),
+                         "traffic": ncu_traffic("k_attn_fwd" + tag, fwd_hash),
                          "peak_note": ((f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 4/3 (Q K^T on the bf16 "
                                         f"path, P V on fp8 at 2 x bf16)") if i8 else
                                        (f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 2 (nominal fp8:bf16);"
@@ -483,7 +485,7 @@ def run_ours(args):
                          "flops_per_launch": flops_step, "ms_per_launch": t_fwd * 1e3},
             "roofline_prepare": {"kernel": "attnq_prepare (all passes)", "bound": "hbm", "achieved": prep_gbs,
                                  "peak": peaks["hbm"], "unit": "GB/s", "frac": prep_gbs / peaks["hbm"],
-                                 "traffic": ncu_traffic("attnq_prepare", prep_hash),
+                                 "traffic": ncu_traffic("attnq_prepare" + tag, prep_hash),
                                  "bytes_per_launch": prep_bytes, "ms_per_launch": t_prep * 1e3},
             "err_vs_fp64": err_sample,
             "cpu_baseline": cpu,
