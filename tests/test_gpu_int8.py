@@ -118,3 +118,33 @@ def test_fwd_int8_dot_products_are_exact_through_cancellation():
     flat["k8"][..., 0] = 0  # every score 0: the sums without their small term
     ref_flat, _ = oracle.attn_quant(flat, (B, Hq, Hkv, N, d), I8, 256.0, 0, True, T)
     assert rel_f(ref_flat, ref).min() > 0.1
+
+
+def test_int8_long_context_full_size_sampled():
+    """The long-context workload at full size with INT8 Q/K: every operand byte and
+    descale against the oracle, and sampled output rows within the forward tolerance."""
+    import torch
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, oracle_bf16, rel_f
+    wl = synth.WORKLOADS["long_context"]
+    B, Hq, Hkv, N, d, T = wl["B"], wl["Hq"], wl["Hkv"], wl["N"], wl["d"], wl["kv_tile"]
+    q, k, v = synth.long_context_inputs(5100, B, Hq, Hkv, N, d)
+    signs = synth.hadamard_signs(17, d)
+    flags = 3 | I8
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    O, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, T, out_dtype=torch.bfloat16, count=False)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs)
+    for name in ("q8", "k8"):
+        # the codes are exact integers in bf16: compare their values
+        assert torch.equal(getattr(bufs, name).float().cpu(), torch.from_numpy(prep[name]).float()), name
+    v8 = bufs.v8[..., :N].transpose(-1, -2).contiguous().cpu()
+    assert torch.equal(v8, torch.from_numpy(prep["v8"]))
+    for key, t in (("q_descale", bufs.scales.q_descale), ("k_descale", bufs.scales.k_descale),
+                   ("v_descale", bufs.scales.v_descale), ("k_mean", bufs.scales.k_mean)):
+        assert np.array_equal(t.cpu().numpy().view(np.uint32), prep[key].view(np.uint32)), key
+    rows = np.array([0, 1, 127, 128, 4095, 16383, 16384, 24577, 32640, 32767], dtype=np.int32)
+    bh = [0, 5, 31, 32, 63]
+    emu, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, 1, True, T, bh_list=bh, rows=rows)
+    got = o_to_numpy(O).reshape(B * Hq, N, d)[bh][:, rows]
+    assert rel_f(got, oracle_bf16(emu)).max() <= REL_F_TOL

@@ -104,3 +104,35 @@ def test_fwd_on_prefix_statistics_matches_oracle(order, flags):
     assert rel_f(o_to_numpy(O).reshape(B * Hq, N, d), ref).max() <= REL_F_TOL
     tot, totr = uf.sum(axis=0).astype(np.int64), ufr.sum(axis=0).astype(np.int64)
     assert np.all(np.abs(tot - totr) <= 0.001 * totr + 2), (tot, totr)
+
+
+def test_prefix_long_context_full_size_sampled():
+    """The long-context workload at full size with statistics from a 4096-token
+    prompt: every operand byte, descale and the mean key against the oracle, and
+    sampled output rows within the forward tolerance."""
+    import torch
+    import precision_attention_numerics_gb300 as aq
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, oracle_bf16, rel_f
+    wl = synth.WORKLOADS["long_context"]
+    B, Hq, Hkv, N, d, T = wl["B"], wl["Hq"], wl["Hkv"], wl["N"], wl["d"], wl["kv_tile"]
+    P = 4096
+    q, k, v = synth.long_context_inputs(5200, B, Hq, Hkv, N, d)
+    signs = synth.hadamard_signs(17, d)
+    flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs, stat_len=P)
+    assert st == 0
+    O, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, T, out_dtype=torch.bfloat16, count=False)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs, stat_len=P)
+    assert torch.equal(bufs.q8.cpu(), torch.from_numpy(prep["q8"]))
+    assert torch.equal(bufs.k8.cpu(), torch.from_numpy(prep["k8"]))
+    v8 = bufs.v8[..., :N].transpose(-1, -2).contiguous().cpu()
+    assert torch.equal(v8, torch.from_numpy(prep["v8"]))
+    for key, t in (("q_descale", bufs.scales.q_descale), ("k_descale", bufs.scales.k_descale),
+                   ("v_descale", bufs.scales.v_descale), ("k_mean", bufs.scales.k_mean)):
+        assert np.array_equal(t.cpu().numpy().view(np.uint32), prep[key].view(np.uint32)), key
+    rows = np.array([0, 1, 127, 4095, 4096, 16384, 24577, 32767], dtype=np.int32)
+    bh = [0, 7, 40, 63]
+    emu, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, 1, True, T, bh_list=bh, rows=rows)
+    got = o_to_numpy(O).reshape(B * Hq, N, d)[bh][:, rows]
+    assert rel_f(got, oracle_bf16(emu)).max() <= REL_F_TOL
