@@ -24,22 +24,23 @@
 //   warps 4-7  softmax warpgroup 1 (query head h0 + 1)
 //   warps 8-11 control warpgroup (warp 11 only waits at the end)
 //   warp 8     TMA producer: Q tiles once per unit (two buffers, so the next
-//              unit's Q loads during this one), K and V^T tiles through an
-//              NS-stage ring
+//              unit's Q loads during this one, where shared memory allows),
+//              K and V^T tiles through an NS-stage ring
 //   warp 9     TMEM allocator; issues warpgroup 0's MMAs
 //   warp 10    issues warpgroup 1's MMAs (each warpgroup's MMAs are in
 //              order; the two streams do not wait for each other).  The MMA
 //              warps run converged and let one elected lane issue: a lone
 //              lane takes about twice as long per MMA.
 // TMEM columns: S_w at [w*T, w*T+T), O_w at [2T + w*D, 2T + w*D + D).
-// Shared memory: Q[2 buffers][2 warpgroups], P[2 warpgroups][2 buffers] (the
+// Shared memory: Q[QBUF buffers][2 warpgroups], P[2 warpgroups][2 buffers] (the
 // E4M3 probabilities, written by the softmax threads in the 128-byte (or
 // 64-byte) swizzled K-major layout the MMA reads; tile n of a warpgroup uses
 // buffer n % 2, whose previous reader, P.V of tile n-2, is known complete),
 // the K and V^T rings.
 //
 // Pipeline per warpgroup w and tile k:
-//   MMA   S_w(k) = Q_w K(k)^T  (kind::f8f6f4, M=128, N=T, K=32 per instruction)
+//   MMA   S_w(k) = Q_w K(k)^T  (kind::f8f6f4, M=128, N=T, K=32 per instruction;
+//         kind::f16 with K=16 for INT8 codes held in bf16)
 //   SM    load S_w(k) from TMEM, then signal "S read"      -> MMA issues S_w(k+1)
 //   SM    row max, alpha, P*S, E4M3 codes, row sum
 //   SM    write P_w(k) to shared memory; only if some row's alpha != 1, wait
