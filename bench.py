@@ -68,11 +68,23 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
 
 
+def code_lines(text: str) -> str:
+    """Source without // comments and blank lines (what the compiler sees of it)."""
+    out = []
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            out.append(code)
+    return "\n".join(out)
+
+
 def kernel_source_hash(files):
+    """Hash of the kernels' code, blind to comments, so a counter capture stays
+    valid across comment edits and is dropped when the code changes."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "precision_attention_numerics_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "precision_attention_numerics_gb300", "csrc", f)) as fh:
+            h.update(code_lines(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
