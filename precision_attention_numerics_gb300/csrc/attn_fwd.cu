@@ -207,6 +207,9 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
                          uint8_t* sQ, uint8_t* sK, uint8_t* sV, const Bars& br, volatile int* abort_flag) {
   using C = Cfg<D, T, I8>;
   uint32_t it = 0, kc = 0, vc = 0;  // tiles walked, K and V loads issued
+  // L2 priorities: K/V tiles are read again by the units of the other query
+  // tiles of their head; a Q tile is read by its unit only
+  const uint64_t keep = l2_evict_last_policy(), once = l2_evict_first_policy();
   int uc = 0;
   bool ok = true;
   bool q_issued = false;
@@ -219,11 +222,11 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
     mbar_arrive_expect_tx(br.q_full + qb, un.nact * C::QB);
 #pragma unroll
     for (int cb = 0; cb < C::QK_BLOCKS; ++cb) {
-      tma_load_3d(q_dst + cb * (kRows * C::QK_BOX), tq, br.q_full + qb, cb * C::QK_BOX, un.t * kRows,
-                  un.b * p.Hq + un.h0);
+      tma_load_3d_hint(q_dst + cb * (kRows * C::QK_BOX), tq, br.q_full + qb, cb * C::QK_BOX, un.t * kRows,
+                       un.b * p.Hq + un.h0, once);
       if (un.nact == 2)
-        tma_load_3d(q_dst + C::QB + cb * (kRows * C::QK_BOX), tq, br.q_full + qb, cb * C::QK_BOX, un.t * kRows,
-                    un.b * p.Hq + un.h0 + 1);
+        tma_load_3d_hint(q_dst + C::QB + cb * (kRows * C::QK_BOX), tq, br.q_full + qb, cb * C::QK_BOX,
+                         un.t * kRows, un.b * p.Hq + un.h0 + 1, once);
     }
     q_issued = true;
     q_last = uc;
@@ -236,11 +239,12 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
       mbar_arrive_expect_tx(br.k_full + s, C::KB);
 #pragma unroll
       for (int cb = 0; cb < C::QK_BLOCKS; ++cb)
-        tma_load_3d(sK + size_t(s) * C::KB + cb * (T * C::QK_BOX), tk, br.k_full + s, cb * C::QK_BOX, jt * T, zkv);
+        tma_load_3d_hint(sK + size_t(s) * C::KB + cb * (T * C::QK_BOX), tk, br.k_full + s, cb * C::QK_BOX, jt * T,
+                         zkv, keep);
       ++kc;
       if (!wait_or_abort(br.v_empty + s, ph ^ 1u, p.wait_ns, abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(br.v_full + s, C::VB);
-      tma_load_3d(sV + size_t(s) * C::VB, tv, br.v_full + s, jt * T, 0, zkv);
+      tma_load_3d_hint(sV + size_t(s) * C::VB, tv, br.v_full + s, jt * T, 0, zkv, keep);
       ++vc;
     }
   }
@@ -609,6 +613,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       reg_fence32(o);
       if (i < p.N) {
         const int64_t off = (int64_t(bh) * p.N + i) * D + 32 * q;
+        // O is written once: streaming stores (evict first)
         if (p.out_bf16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.O) + off);
 #pragma unroll
@@ -620,14 +625,16 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
                                                               __fmul_rn(__uint_as_float(o[8 * v + 2 * e + 1]), scale));
               wv[e] = *reinterpret_cast<const uint32_t*>(&b2);
             }
-            dst[v] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            __stcs(dst + v, make_uint4(wv[0], wv[1], wv[2], wv[3]));
           }
         } else {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + off);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            dst[v] = make_float4(__fmul_rn(__uint_as_float(o[4 * v]), scale), __fmul_rn(__uint_as_float(o[4 * v + 1]), scale),
-                                 __fmul_rn(__uint_as_float(o[4 * v + 2]), scale), __fmul_rn(__uint_as_float(o[4 * v + 3]), scale));
+            __stcs(dst + v, make_float4(__fmul_rn(__uint_as_float(o[4 * v]), scale),
+                                        __fmul_rn(__uint_as_float(o[4 * v + 1]), scale),
+                                        __fmul_rn(__uint_as_float(o[4 * v + 2]), scale),
+                                        __fmul_rn(__uint_as_float(o[4 * v + 3]), scale)));
           }
         }
       }
