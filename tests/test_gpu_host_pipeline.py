@@ -12,13 +12,12 @@ import synth
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("steps,N,out_bf16", [(1, 300, True), (3, 1000, False), (5, 257, True)])
-def test_host_pipeline_matches_device_path(steps, N, out_bf16):
+def _pipeline_vs_device(steps, N, out_bf16, extra_flags=0, stat_len=0):
     import precision_attention_numerics_gb300 as aq
     B, Hq, Hkv, d, T = 1, 4, 2, 128, 128
-    flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT
+    flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT | extra_flags
     signs = torch.from_numpy(synth.hadamard_signs(21, d)).cuda()
-    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, flags, signs)
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, flags, signs, stat_len)
     odt = aq.ATTNQ_BF16 if out_bf16 else aq.ATTNQ_F32
     tdt = torch.bfloat16 if out_bf16 else torch.float32
     hosts = []
@@ -42,6 +41,21 @@ def test_host_pipeline_matches_device_path(steps, N, out_bf16):
         got = outs[i].view(torch.int16 if out_bf16 else torch.int32).numpy()
         want = O.cpu().view(torch.int16 if out_bf16 else torch.int32).numpy()
         assert np.array_equal(got, want), i
+
+
+@pytest.mark.parametrize("steps,N,out_bf16", [(1, 300, True), (3, 1000, False), (5, 257, True)])
+def test_host_pipeline_matches_device_path(steps, N, out_bf16):
+    _pipeline_vs_device(steps, N, out_bf16)
+
+
+@pytest.mark.parametrize("extra,stat_len", [("i8", 0), ("tile", 300), ("i8+tile", 200), ("i8", 777)])
+def test_host_pipeline_other_options(extra, stat_len):
+    """INT8 Q/K codes take two bytes in the pipeline's operand buffers, per-tile
+    scales one descale per tile, prefix statistics change only the kernels'
+    arguments: every variant still equals the device path bit for bit."""
+    import precision_attention_numerics_gb300 as aq
+    f = {"i8": aq.ATTNQ_I8QK, "tile": aq.ATTNQ_TILE_SCALES, "i8+tile": aq.ATTNQ_I8QK | aq.ATTNQ_TILE_SCALES}[extra]
+    _pipeline_vs_device(3, 1000, True, f, stat_len)
 
 
 def test_host_pipeline_rejects_bad_arguments():
