@@ -87,6 +87,35 @@ def test_prepare_cast_covers_every_float_up_to_448():
         assert np.array_equal(got[rows * d: rows * d + n], ref_pos | np.uint8(0x80)), start
 
 
+def test_prepare_cast_saturates_every_finite_float_above_448():
+    """With statistics from a first token whose amax is 448 the scale is 1 and
+    later tokens reach the cast unscaled: every finite float32 above 448 (and
+    its negation) must encode as the oracle's encoder does, i.e. saturate."""
+    from tests.gpu_helpers import gpu_prepare
+    d = 128
+    lo = int(np.float32(448.0).view(np.uint32)) + 1
+    hi = int(np.float32(np.finfo(np.float32).max).view(np.uint32))
+    chunk = 1 << 26
+    for start in range(lo, hi + 1, chunk):
+        n = min(chunk, hi + 1 - start)
+        vals = np.arange(start, start + n, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        rows = (n + d - 1) // d
+        flat = np.zeros((1 + 2 * rows) * d, np.float32)
+        flat[0] = 448.0  # the statistics token
+        flat[d: d + n] = vals
+        flat[(1 + rows) * d: (1 + rows) * d + n] = -vals
+        v = flat.reshape(1, 1, 1 + 2 * rows, d)
+        q = np.ones_like(v)
+        desc, bufs, status = gpu_prepare(q, q, v, 0, None, vt=False, stat_len=1)
+        assert status == 0
+        assert float(bufs.scales.v_descale[0]) == 1.0
+        got = bufs.v8.cpu().numpy().reshape(-1)
+        ref_pos = oracle.e4m3_encode_bits(start, n)
+        assert np.all(ref_pos == 0x7E)
+        assert np.array_equal(got[d: d + n], ref_pos), start
+        assert np.array_equal(got[(1 + rows) * d: (1 + rows) * d + n], ref_pos | np.uint8(0x80)), start
+
+
 @pytest.mark.parametrize("bad", [np.nan, np.inf, -np.inf])
 def test_prepare_reports_nonfinite(bad):
     from tests.gpu_helpers import gpu_prepare
