@@ -148,3 +148,31 @@ def test_int8_long_context_full_size_sampled():
     emu, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, 1, True, T, bh_list=bh, rows=rows)
     got = o_to_numpy(O).reshape(B * Hq, N, d)[bh][:, rows]
     assert rel_f(got, oracle_bf16(emu)).max() <= REL_F_TOL
+
+
+def test_int8_cast_of_every_finite_float():
+    """With statistics from a first token whose amax is 127 the INT8 scale is 1,
+    so later tokens reach the cast unscaled: every finite float32 (both signs)
+    must give the oracle's code, nearest integer with ties to even, saturated."""
+    import torch
+    from tests.gpu_helpers import gpu_prepare
+    d = 128
+    hi = int(np.float32(np.finfo(np.float32).max).view(np.uint32))
+    chunk = 1 << 26
+    for start in range(0, hi + 1, chunk):
+        n = min(chunk, hi + 1 - start)
+        vals = np.arange(start, start + n, dtype=np.uint32).view(np.float32)
+        rows = (n + d - 1) // d
+        flat = np.zeros((1 + 2 * rows) * d, np.float32)
+        flat[0] = 127.0  # the statistics token
+        flat[d: d + n] = vals
+        flat[(1 + rows) * d: (1 + rows) * d + n] = -vals
+        q = flat.reshape(1, 1, 1 + 2 * rows, d)
+        ones = np.ones_like(q)
+        desc, bufs, status = gpu_prepare(q, ones, ones, I8, None, vt=False, stat_len=1)
+        assert status == 0
+        assert float(bufs.scales.q_descale[0]) == 1.0
+        got = bufs.q8.to(torch.int8).cpu().numpy().reshape(-1)
+        want = oracle.int8_encode(vals)
+        assert np.array_equal(got[d: d + n], want), start
+        assert np.array_equal(got[(1 + rows) * d: (1 + rows) * d + n], oracle.int8_encode(-vals)), start

@@ -98,7 +98,7 @@ def test_prepare_cast_saturates_every_finite_float_above_448():
     chunk = 1 << 26
     for start in range(lo, hi + 1, chunk):
         n = min(chunk, hi + 1 - start)
-        vals = np.arange(start, start + n, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        vals = np.arange(start, start + n, dtype=np.uint32).view(np.float32)
         rows = (n + d - 1) // d
         flat = np.zeros((1 + 2 * rows) * d, np.float32)
         flat[0] = 448.0  # the statistics token
