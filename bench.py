@@ -58,6 +58,11 @@ def prepare_bytes(B, Hq, Hkv, N, d, in_bytes=2, qk_code_bytes=1):
     return elems * in_bytes + (elems - qk) + qk * qk_code_bytes
 
 
+# Dense tensor peaks from the datasheet, TFLOP/s: FP8 for the E4M3 step; for
+# INT8-QK half the flops run on the bf16 path, so 1 / (0.5 / 2250 + 0.5 / 4500).
+DATASHEET_MMA_TFLOPS = {"e4m3": 4500.0, "int8": 3000.0}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -494,7 +499,10 @@ def run_ours(args):
                                         f"path, P V on fp8 at 2 x bf16)") if i8 else
                                        (f"{peaks['source']} bf16 sustained {peaks['bf16_sus']} x 2 (nominal fp8:bf16);"
                                         f" burst-based peak {fp8_peak_burst:.1f}")),
-                         "flops_per_launch": flops_step, "ms_per_launch": t_fwd * 1e3},
+                         "flops_per_launch": flops_step, "ms_per_launch": t_fwd * 1e3,
+                         # the dense datasheet figure, for context (GB300: 4.5 PFLOP/s FP8, 2.25 bf16)
+                         "datasheet": {"peak": DATASHEET_MMA_TFLOPS["int8" if i8 else "e4m3"],
+                                       "frac": fwd_tflops / DATASHEET_MMA_TFLOPS["int8" if i8 else "e4m3"]}},
             "roofline_prepare": {"kernel": "attnq_prepare (all passes)", "bound": "hbm", "achieved": prep_gbs,
                                  "peak": peaks["hbm"], "unit": "GB/s", "frac": prep_gbs / peaks["hbm"],
                                  "traffic": ncu_traffic("attnq_prepare" + tag, prep_hash),
