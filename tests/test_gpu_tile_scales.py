@@ -58,3 +58,29 @@ def test_fwd_tile_scales_matches_oracle(order, T, N):
     assert rel_f(o_to_numpy(O).reshape(B * Hq, N, d), ref).max() <= REL_F_TOL
     tot, totr = uf.sum(axis=0).astype(np.int64), ufr.sum(axis=0).astype(np.int64)
     assert np.all(np.abs(tot - totr) <= 0.001 * totr + 2), (tot, totr)
+
+
+@pytest.mark.parametrize("i8", [False, True])
+@pytest.mark.parametrize("T", [64, 128])
+def test_tile_instance_with_equal_tile_scales_equals_slice_instance(i8, T):
+    """Per-tile logit factors reduce to the per-slice one when every tile
+    carries the slice's descale: the per-tile forward then gives the slice
+    forward's output bit for bit."""
+    import torch
+    import precision_attention_numerics_gb300 as aq
+    from tests.gpu_helpers import gpu_fwd, gpu_prepare
+    B, Hq, Hkv, N, d = 1, 4, 2, 1000, 128
+    q, k, v = synth.qwen_like_inputs(990 + T + i8, B, Hq, Hkv, N, d, key_norm=30.0, key_channels=4)
+    signs = synth.hadamard_signs(93, d)
+    flags = 3 | (aq.ATTNQ_I8QK if i8 else 0)
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    O1, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, T, out_dtype=torch.float32, count=False)
+    assert st == 0
+    nt = aq.attnq_scale_tiles(N)
+    tdesc = aq.AttnqDesc(B, Hq, Hkv, N, d, desc.in_dtype, desc.flags | TILE, desc.signs)
+    bufs.scales = aq.AttnqScales(bufs.scales.q_descale.repeat_interleave(nt),
+                                 bufs.scales.k_descale.repeat_interleave(nt), bufs.scales.v_descale, None)
+    O2, _, st = gpu_fwd(tdesc, bufs, 256.0, 1, True, T, out_dtype=torch.float32, count=False)
+    assert st == 0
+    assert torch.equal(O1, O2)
