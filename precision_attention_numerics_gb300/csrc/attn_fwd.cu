@@ -11,8 +11,10 @@
 // skipped rescale with alpha == 1 is exact).
 // Arithmetic per score (two at a time with the packed f32x2 instructions):
 // the row maximum is taken on the raw q8.k8 sums (scaling by c > 0 commutes
-// with rounding and max), then P*S = 2^(fma(s, c, log2 S - m')) comes out of
-// one ex2, and the row sum accumulates P*S (= S*l, divided out at the end).
+// with rounding and max) - on tiles without a masked key it comes with the S
+// load itself (tcgen05.ld.red, sm_103a) - then P*S = 2^(fma(s, c, log2 S - m'))
+// comes out of one ex2, and the row sum accumulates P*S (= S*l, divided out
+// at the end).
 //
 // Work unit: one 128-row query tile of two query heads that share a KV head
 // (GQA); both use the same K/V tiles and the same KV range.  A persistent
@@ -470,48 +472,63 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       const bool need_mask = (p.causal && j0 + T - 1 > un.t * kRows) || (j0 + T > p.N);
       // keys j0 + j are visible for j < lim (causal: j0 + j <= i; always j0 + j < N)
       const int lim = need_mask ? min(p.N - j0, p.causal ? i - j0 + 1 : T) : T;
-      // S in two halves: the row max of the first half runs while the second
-      // half is still on its way out of TMEM
       constexpr int H = T / 2;
       float sv[T];
+      float smax;
+      if (!need_mask) {
+        // No key of the tile is masked: tcgen05.ld.red returns the maximum of
+        // each 32-column load with the values, so the row max is the maximum
+        // of T/32 numbers (the same value the software chains give).
+        float hm[T / 32];
 #pragma unroll
-      for (int q = 0; q < H / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
-      tmem_wait_ld();
+        for (int q = 0; q < T / 32; ++q)
+          tmem_ld32f_max(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]), hm[q]);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < H / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+        for (int q = 0; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+        // S_w is in registers: the MMA warp may overwrite it with the next tile
+        tc_fence_before();
+        mbar_arrive(br.s_free + w);
+        smax = hm[0];
 #pragma unroll
-      for (int q = H / 32; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
-      if (need_mask) {
+        for (int q = 1; q < T / 32; ++q) smax = fmaxf(smax, hm[q]);
+      } else {
+        // Diagonal or ragged tile: masked keys must not enter the maximum, so
+        // S comes in two halves and the row max of the masked first half runs
+        // while the second half is still on its way out of TMEM.
+#pragma unroll
+        for (int q = 0; q < H / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < H / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+#pragma unroll
+        for (int q = H / 32; q < T / 32; ++q) tmem_ld32f(tS + uint32_t(32 * q), *reinterpret_cast<float(*)[32]>(&sv[32 * q]));
 #pragma unroll
         for (int j = 0; j < H; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
-      }
-      // row max of the raw sums (fl32(s * c) is monotone in s for c > 0):
-      // eight independent two-input chains (the three-input form measured slower)
-      float mx[8];
+        // row max of the raw sums (fl32(s * c) is monotone in s for c > 0):
+        // eight independent two-input chains (the three-input form measured slower)
+        float mx[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = sv[e];
+        for (int e = 0; e < 8; ++e) mx[e] = sv[e];
 #pragma unroll
-      for (int j = 8; j < H; j += 8) {
+        for (int j = 8; j < H; j += 8) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
-      }
-      tmem_wait_ld();
+          for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
+        }
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = H / 32; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
-      // S_w is in registers: the MMA warp may overwrite it with the next tile
-      tc_fence_before();
-      mbar_arrive(br.s_free + w);
-      if (need_mask) {
+        for (int q = H / 32; q < T / 32; ++q) reg_fence32(*reinterpret_cast<float(*)[32]>(&sv[32 * q]));
+        tc_fence_before();
+        mbar_arrive(br.s_free + w);
 #pragma unroll
         for (int j = H; j < T; ++j) sv[j] = (j < lim) ? sv[j] : -INFINITY;
-      }
 #pragma unroll
-      for (int j = H; j < T; j += 8) {
+        for (int j = H; j < T; j += 8) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
+          for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], sv[j + e]);
+        }
+        smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       }
-      const float smax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float mt = (smax == -INFINITY) ? -INFINITY : __fmul_rn(smax, c);
       const float mnew = fmaxf(m, mt);
       const float muse = (mnew == -INFINITY) ? 0.0f : mnew;
