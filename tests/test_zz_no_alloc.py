@@ -25,13 +25,13 @@ def _outputs(bufs):
             bufs.scales.k_mean]
 
 
-def _both(q, k, v, flags, signs):
+def _both(q, k, v, flags, signs, stat_len=0):
     import precision_attention_numerics_gb300 as aq
     from tests.gpu_helpers import dev
     B, Hq, N, d = q.shape
     in_dtype = aq.ATTNQ_BF16 if q.dtype == np.uint16 else aq.ATTNQ_F32
     sg = None if signs is None else torch.from_numpy(signs).cuda()
-    desc = aq.AttnqDesc(B, Hq, k.shape[1], N, d, in_dtype, flags | aq.ATTNQ_VT_LAYOUT, sg)
+    desc = aq.AttnqDesc(B, Hq, k.shape[1], N, d, in_dtype, flags | aq.ATTNQ_VT_LAYOUT, sg, stat_len)
     Q, K, V = dev(q), dev(k), dev(v)
     ref = aq.alloc_prepared(desc)
     aq.attnq_prepare(desc, Q, K, V, ref.q8, ref.k8, ref.v8, ref.scales, ref.workspace)
@@ -79,3 +79,12 @@ def test_static_scratch_rejects_too_large_before_launch():
     d_c, s_c = desc._c(), scales._c()
     rc = L.attnq_prepare_static(C.byref(d_c), fake, fake, fake, fake, fake, fake, C.byref(s_c), None)
     assert rc == 2
+
+
+@pytest.mark.parametrize("flags,stat_len", [(3 | 16, 0), (3, 400), (3 | 16 | 8, 300)])
+def test_static_scratch_with_other_forms(flags, stat_len):
+    """INT8 Q/K codes, causal-prefix statistics and per-tile scales through the
+    fixed scratch: bit for bit the workspace entry point's outputs."""
+    d = 128
+    q, k, v = synth.qwen_like_inputs(40 + stat_len, 1, 4, 2, 1000, d, key_norm=30.0, key_channels=4)
+    _both(q, k, v, flags, synth.hadamard_signs(4, d), stat_len)
