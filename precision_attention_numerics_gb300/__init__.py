@@ -3,10 +3,26 @@ attention-numerics pages: optional random-sign Hadamard rotation of Q and K,
 optional mean-key subtraction, per-(batch, head) max-based E4M3 scales, online
 softmax over KV tiles in forward or reverse order, and a static P-cast scale S.
 
+Further options: per-128-token-tile Q/K scales (ATTNQ_TILE_SCALES), mean key
+and slice scales from the first stat_len tokens (AttnqDesc.stat_len), and
+INT8 Q/K codes with FP8 P and V (ATTNQ_I8QK).
+
 The compute lives in libattnq.so (hand-written CUDA kernels behind a C ABI,
 include/attnq.h).  This package is a thin ctypes binding with the same names
 as the C functions; it only marshals arguments.  There is no CPU fallback:
 every call raises if the library has not been built.
+
+Typical use (device tensors from torch; Q [B,Hq,N,d], K and V [B,Hkv,N,d] bf16):
+
+    import precision_attention_numerics_gb300 as aq
+    signs = torch.from_numpy(aq.attnq_hadamard_signs(seed, d)).cuda()
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16,
+                        aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT, signs)
+    bufs = aq.alloc_prepared(desc)
+    aq.attnq_prepare(desc, Q, K, V, bufs.q8, bufs.k8, bufs.v8, bufs.scales, bufs.workspace)
+    O = torch.empty(B, Hq, N, d, dtype=torch.bfloat16, device="cuda")
+    aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, 256.0, aq.ATTNQ_KV_REVERSE, True, 128, O)
+    assert aq.attnq_device_status() == 0
 """
 from .binding import (  # noqa: F401
     ATTNQ_BF16,
