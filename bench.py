@@ -15,6 +15,12 @@ memory and its output back inside the timed region, the copies of
 neighbouring steps overlapping each step's kernels.  Under torchrun every rank runs its own independent replica
 (weak scaling, no collective on the data path).
 
+Variants of the same workload (not the default line): --qk int8 (INT8 Q/K
+codes, Q.K^T on the bf16 tensor path; the roofline peak is then 4/3 of bf16),
+--stat-len P (mean key and slice scales from the first P tokens), --scales
+tile (per-128-token Q/K scales); --report harm times the four-condition harm
+report on one Qwen-0.5B-shaped layer instead.
+
 --impl reference times the CPU oracle (the plain C++ implementation used by
 the tests) on a bounded sample of the same workload.
 """
