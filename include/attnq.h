@@ -27,6 +27,10 @@
  *    and launch errors found before or at launch.  Errors found on the device
  *    (non-finite input, a wait that timed out) are recorded in a per-device
  *    status word and reported by attnq_device_status().
+ *  - The library caches, per device, the device addresses of its status word
+ *    and of the attnq_prepare_static scratch array.  cudaDeviceReset destroys
+ *    the context they belong to: after it the library must not be used again
+ *    in that process.
  *  - No C++ exception crosses this interface.  Functions are thread-safe for
  *    distinct streams except where stated.
  *  - Requires an sm_103 device; other devices give ATTNQ_EUNSUPPORTED.
@@ -211,7 +215,16 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
  *   l = alpha * l + sum_j P_j;  p8_j = E4M3(P_j * S);
  *   acc = alpha * acc + sum_j p8_j * v8_j;
  * and finally O = acc * dv / (S * l).  The running maximum is exact (no
- * lazy rescaling).  With ATTNQ_TILE_SCALES, dq is row i's query tile's and dk
+ * lazy rescaling).  The kernel evaluates P_j * S in one step, as
+ * 2^(fma(s_j, c, log2 S - m')) with ex2.approx (exact 2^x for S a power of
+ * two; for other S, log2 S rounded to fp32), and its row sum accumulates
+ * P_j * S, which equals S * l up to rounding; the cast and the division by
+ * S * l are as stated.  E4M3 codes, and so the underflow counts, can
+ * therefore differ from the literal two-step P then P * S where P * S lies
+ * within a few ulp of a rounding boundary.  A factor c below the smallest
+ * normal float (FLT_MIN) is raised to FLT_MIN: every logit is then below
+ * 2^-100 in magnitude either way (|s_j| < 2^25) and every P is 1 in fp32, so no result
+ * changes, and masked keys keep P * S = 0.  With ATTNQ_TILE_SCALES, dq is row i's query tile's and dk
  * key j's tile's descale (kv_tile divides the scale tile, so c is constant
  * within a KV tile).  desc: shape and flags of the attnq_prepare call that made
  * the operands (ATTNQ_VT_LAYOUT is required; in_dtype is ignored).

@@ -61,6 +61,7 @@
 // drained (again with a bound) and TMEM is freed before the CTA exits.
 #include <cuda_bf16.h>
 
+#include <cfloat>
 #include <cmath>
 
 #include "internal.h"
@@ -447,7 +448,11 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
     const float cq = __double2float_rn(__dmul_rn(__dmul_rn(__dmul_rn(dq, p.inv_sqrt_d), p.rot), p.log2e));
     const float* kd = TILES ? p.k_ds + int64_t(bg) * p.n_st : p.k_ds + bg;
     auto key_scale_tile = [&](int k) { return ((p.reverse ? un.nt - 1 - k : k) * T) / kScaleTile; };
-    float c = __fmul_rn(cq, kd[TILES ? key_scale_tile(0) : 0]);
+    // A factor below the smallest normal float (Q and K descales near 1e-20
+    // or less) makes every logit smaller than 2^-100 (|s| < 2^25), so every P is 1 in fp32
+    // either way; raising c to FLT_MIN there changes no P and keeps the
+    // masked keys' -inf * c at -inf (0 * -inf would be NaN).
+    float c = fmaxf(__fmul_rn(cq, kd[TILES ? key_scale_tile(0) : 0]), FLT_MIN);
     float dk_next = 0.0f;
     if constexpr (TILES) {
       if (un.nt > 1) dk_next = kd[key_scale_tile(1)];
@@ -464,7 +469,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
       tc_fence_after();
       if constexpr (TILES) {
         if (k > 0) {
-          c = __fmul_rn(cq, dk_next);
+          c = fmaxf(__fmul_rn(cq, dk_next), FLT_MIN);
           c2 = pack2(c, c);
           if (k + 1 < un.nt) dk_next = kd[key_scale_tile(k + 1)];
         }

@@ -190,3 +190,32 @@ CONDITIONS = {  # name -> (rotate, center_k)
     "centred": (False, True),
     "centred_rotated": (True, True),
 }
+
+
+# Seeds of the workloads' instances: 1000 * workload index + sub-index.
+SEED_BASE = {"sink_probe": 1000, "pcast_sweep": 2000, "qwen05b": 3000, "qwen15b": 4000, "long_context": 5000}
+
+
+def sink_probe_inputs():
+    """The sink probe's one instance (delta = 7)."""
+    wl = WORKLOADS["sink_probe"]
+    return sink_inputs(SEED_BASE["sink_probe"] + 1, wl["B"], wl["Hq"], wl["N"], wl["d"], delta=wl["deltas"][0])
+
+
+def pcast_sweep_inputs(delta: float, N: int | None = None):
+    """One delta of the P-cast sweep (float32, 8 heads); N defaults to the sweep's 4096."""
+    wl = WORKLOADS["pcast_sweep"]
+    return sink_inputs(SEED_BASE["pcast_sweep"] + int(delta), wl["B"], wl["Hq"], wl["N"] if N is None else N,
+                       wl["d"], delta=float(delta))
+
+
+def qwen_layer_inputs(name: str, layer: int):
+    """Layer `layer` of a Qwen-shaped workload ("qwen05b" or "qwen15b"): bf16 bit patterns."""
+    wl = WORKLOADS[name]
+    return qwen_like_inputs(SEED_BASE[name] + layer, wl["B"], wl["Hq"], wl["Hkv"], wl["N"], wl["d"],
+                            key_norm=wl["key_norm"], key_channels=wl["key_channels"])
+
+
+def qwen_signs(name: str):
+    """The fixed Hadamard sign vector of a Qwen-shaped workload (one for all its layers)."""
+    return hadamard_signs(SEED_BASE[name] + 1, WORKLOADS[name]["d"])

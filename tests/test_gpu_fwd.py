@@ -76,6 +76,22 @@ def test_bf16_output():
     _run(q, k, v, 3, 256.0, 1, True, 128, out_dtype=torch.bfloat16, signs=synth.hadamard_signs(4, 128))
 
 
+def test_logit_factor_underflow_stays_finite():
+    """Q and K near 1e-21 (bf16): the descales are near 1e-23, so the logit
+    factor c = fl32(cq * dk) underflows to 0, every logit is 0 and attention
+    is uniform over the visible keys.  Masked keys of the diagonal tiles must
+    still give P * S = 0 (no 0 * infinity)."""
+    q, k, v = synth.qkv_normal(98, 1, 2, 2, 300, 64)
+    q, k = q * np.float32(1e-21), k * np.float32(1e-21)
+    q, k, v = (synth.to_bf16_bits(x) for x in (q, k, v))
+    for T in (64, 128):
+        _run(q, k, v, 0, 256.0, 1, True, T)
+
+
+# S = 448 is not a power of two: the kernel forms P * S as one ex2 of
+# fma(s, c, log2 S - m') with log2 S rounded to fp32, so a P * S within an ulp
+# or two of the 2^-10 threshold can land on the other side of it than the
+# oracle's two-step P then P * S; the 0.1% + 2 bar covers those.
 @pytest.mark.parametrize("S", [1.0, 256.0, 448.0])
 def test_pcollapse_counts_forward(S):
     q, k, v = synth.sink_inputs(95, 1, 2, 1024, 128, delta=9.0)

@@ -5,7 +5,11 @@ against the oracle:
   rotated, centred, centred + rotated): forward parity with the quantised
   emulation (rel-F <= 2e-3) and each head's log1p error against FP64 within
   5% of the oracle's (attnq_err with the oracle's exact attention as O_ref);
-* the P-cast sweep shape at its full length N = 4096 (P-only mode);
+* the P-cast sweep at its full size (N = 4096, 8 heads, P-only mode) for all
+  six (order, S) pairs at delta in {0, 4, 7, 10, 12}: outputs within rel-F
+  2e-3 of the oracle and underflow counts within 0.1% + 2;
+* every layer of both Qwen-shaped workloads (24 and 28) in all four
+  conditions (marked slow: about five minutes of oracle time);
 * the long-context workload at full size in the configuration bench.py times
   (B=2, Hq=32, Hkv=8, N=32768, d=128, rotation + centring, reverse, S=256,
   bf16 output): every E4M3 operand byte, descale and mean-key value, and the
@@ -27,16 +31,13 @@ def _flags(rotate, center):
     return (1 if rotate else 0) | (2 if center else 0)
 
 
-@pytest.mark.parametrize("name", ["qwen05b", "qwen15b"])
-def test_qwen_shaped_layer_all_conditions(name):
+def _qwen_layer_all_conditions(name, layer):
     import precision_attention_numerics_gb300 as aq
     from tests.gpu_helpers import ERR_REL_TOL, REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, rel_f
     wl = synth.WORKLOADS[name]
     B, Hq, Hkv, N, d, T = wl["B"], wl["Hq"], wl["Hkv"], wl["N"], wl["d"], wl["kv_tile"]
-    seed = 3000 if name == "qwen05b" else 4000
-    q, k, v = synth.qwen_like_inputs(seed, B, Hq, Hkv, N, d, key_norm=wl["key_norm"],
-                                     key_channels=wl["key_channels"])
-    signs = synth.hadamard_signs(seed + 1, d)
+    q, k, v = synth.qwen_layer_inputs(name, layer)
+    signs = synth.qwen_signs(name)
     exact = oracle.attn_exact(q, k, v)
     Oref = torch.from_numpy(exact.reshape(B, Hq, N, d)).cuda()
     errs = {}
@@ -61,13 +62,28 @@ def test_qwen_shaped_layer_all_conditions(name):
     assert np.all(np.isfinite(harm))
 
 
-@pytest.mark.parametrize("order,S", [(0, 1.0), (1, 256.0)])
-def test_pcast_sweep_full_length(order, S):
+@pytest.mark.parametrize("name", ["qwen05b", "qwen15b"])
+def test_qwen_shaped_layer_all_conditions(name):
+    _qwen_layer_all_conditions(name, 0)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,layer", [("qwen05b", x) for x in range(1, synth.WORKLOADS["qwen05b"]["layers"])]
+                         + [("qwen15b", x) for x in range(1, synth.WORKLOADS["qwen15b"]["layers"])])
+def test_qwen_shaped_every_layer(name, layer):
+    """Layers 1.. of both Qwen-shaped workloads (layer 0 is the test above)."""
+    _qwen_layer_all_conditions(name, layer)
+
+
+@pytest.mark.parametrize("delta", [0.0, 4.0, 7.0, 10.0, 12.0])
+@pytest.mark.parametrize("order,S", [(0, 1.0), (0, 256.0), (0, 448.0), (1, 1.0), (1, 256.0), (1, 448.0)])
+def test_pcast_sweep_full_size(order, S, delta):
     from tests.gpu_helpers import rel_f
     import precision_attention_numerics_gb300 as aq
     from tests.gpu_helpers import dev
-    B, H, N, d, T = 1, 8, 4096, 128, 128
-    q, k, v = synth.sink_inputs(2007, B, H, N, d, delta=7.0)
+    wl = synth.WORKLOADS["pcast_sweep"]
+    B, H, N, d, T = wl["B"], wl["Hq"], wl["N"], wl["d"], wl["kv_tile"]
+    q, k, v = synth.pcast_sweep_inputs(delta)
     desc = aq.AttnqDesc(B, H, H, N, d, aq.ATTNQ_F32, 0, None)
     O = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
     uf = torch.zeros(B * H * 2, dtype=torch.int64, device="cuda")

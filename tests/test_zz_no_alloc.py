@@ -70,15 +70,25 @@ def test_static_scratch_long_context_shape_fits():
 
 def test_static_scratch_rejects_too_large_before_launch():
     import precision_attention_numerics_gb300 as aq
-    # 64 KV heads x 1024 chunks of 128 tokens x 128 channels of fp32 partial sums: 32 MiB > the array
-    desc = aq.AttnqDesc(1, 64, 64, 131072, 128, aq.ATTNQ_BF16, aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT)
+    # 16 KV heads x 512 chunks of 128 tokens x 128 channels of fp32 partial
+    # sums: just over 4 MiB, more than the array holds
+    B, Hq, Hkv, N, d = 1, 16, 16, 65536, 128
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT)
     assert aq.attnq_prepare_workspace(desc) > aq.ATTNQ_STATIC_SCRATCH_BYTES
+    # every buffer is a real allocation of the size the descriptor implies,
+    # so nothing passed here points outside memory this process owns
+    bufs = aq.alloc_prepared(desc)
+    Q = torch.zeros((B, Hq, N, d), dtype=torch.bfloat16, device="cuda")
+    K = torch.zeros((B, Hkv, N, d), dtype=torch.bfloat16, device="cuda")
+    V = torch.zeros((B, Hkv, N, d), dtype=torch.bfloat16, device="cuda")
     L = aq.load_library()
-    fake = C.c_void_p(1 << 20)   # never dereferenced: the size check comes first
-    scales = aq.AttnqScales(*(torch.empty(1, device="cuda") for _ in range(3)))
-    d_c, s_c = desc._c(), scales._c()
-    rc = L.attnq_prepare_static(C.byref(d_c), fake, fake, fake, fake, fake, fake, C.byref(s_c), None)
+    d_c, s_c = desc._c(), bufs.scales._c()
+    rc = L.attnq_prepare_static(C.byref(d_c), *(C.c_void_p(t.data_ptr()) for t in (Q, K, V, bufs.q8, bufs.k8,
+                                                                                   bufs.v8)),
+                                C.byref(s_c), C.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == 2
+    # nothing was launched: the outputs are as allocated and the device is clean
+    assert aq.attnq_device_status() == 0
 
 
 @pytest.mark.parametrize("flags,stat_len", [(3 | 16, 0), (3, 400), (3 | 16 | 8, 300)])
