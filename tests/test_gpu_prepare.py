@@ -128,3 +128,39 @@ def test_prepare_reports_nonfinite(bad):
     q2, k2, v2 = synth.qkv_normal(3, 1, 2, 1, 64, 64)
     _, _, status = gpu_prepare(q2, k2, v2, 3, synth.hadamard_signs(1, 64))
     assert status == 0       # the status word was cleared by the last read
+
+
+def _bf16_inputs(qf, kf, vf):
+    return tuple(synth.to_bf16_bits(np.ascontiguousarray(x, dtype=np.float32)) for x in (qf, kf, vf))
+
+
+@pytest.mark.parametrize("case", ["near_ties", "late_outlier", "wide_range", "tiny", "small"])
+def test_rotated_amax_edge_cases(case):
+    """The amax of rotated, uncentred bf16 slices (d = 128) is the maximum of
+    the exact butterfly outputs over all rows, whatever row or tile holds it;
+    scales and codes must equal the oracle's bit for bit.  Cases: rows whose
+    rotated maxima nearly tie (copies of one row, one element nudged by about
+    a bf16 ulp), the slice maximum in a single late row, rows mixing
+    magnitudes 2^20 and 2^-20, and slices of values near 1e-33 and 1e-28."""
+    d, N = 128, 1000
+    rng = np.random.default_rng(17)
+    qf, kf, vf = (x.astype(np.float64) for x in synth.qkv_normal(31, 1, 4, 2, N, d))
+    if case == "near_ties":
+        base = qf[0, 0, 0].copy()
+        for h in range(4):
+            for t in range(N):
+                row = base.copy()
+                row[(7 * t + h) % d] *= 1.0 + 2.0 ** -7 * ((t % 3) - 1)
+                qf[0, h, t] = row
+    elif case == "late_outlier":
+        qf[0, :, N - 3] *= 6.0
+        kf[0, :, N - 1] *= 9.0
+    elif case == "wide_range":
+        scale = np.where(rng.random((1, 4, N, d)) < 0.5, 2.0 ** 20, 2.0 ** -20)
+        qf = qf * scale
+    elif case == "tiny":
+        qf, kf = qf * 1e-33, kf * 1e-33
+    elif case == "small":
+        qf, kf = qf * 1e-28, kf * 1e-28
+    q, k, v = _bf16_inputs(qf, kf, vf)
+    _check_prepare(q, k, v, 1, synth.hadamard_signs(15, d))
