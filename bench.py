@@ -890,6 +890,7 @@ def run_ours(args):
     prep_bytes = prepare_bytes(B, Hq, Hkv, N, d, qk_code_bytes=2 if i8 else 1)
     prep_gbs = prep_bytes / t_prep / 1e9
     fwd_hash = kernel_source_hash(["attn_fwd.cu", "ptx.cuh"])
+    full_size = (B, Hq, Hkv) == (2, 32, 8)  # the captures are of the full workload
     # traffic is recorded per kernel and per workload variant
     tag = ("_i8" if i8 else "") + ("_tile" if args.scales == "tile" else "") + (f"_p{args.stat_len}" if args.stat_len else "")
     prep_hash = kernel_source_hash(["prepare.cu", "ptx.cuh"])
@@ -936,7 +937,7 @@ def run_ours(args):
             "fp8_gemm_peak": fp8_meas,
             "roofline": {"kernel": "attnq_fwd (k_attn_fwd<128,128>)", "bound": "tensor", "achieved": fwd_tflops,
                          "peak": mma_peak, "unit": "TFLOP/s", "frac": fwd_tflops / mma_peak,
-                         "traffic": ncu_traffic("k_attn_fwd" + tag, fwd_hash),
+                         "traffic": ncu_traffic("k_attn_fwd" + tag, fwd_hash) if full_size else None,
                          "peak_note": ((f"1 / (0.5 / bf16 burst {peaks['bf16']} + 0.5 / fp8 {fp8_peak:.1f}): Q K^T on "
                                         f"the bf16 path, P V on fp8; fp8 {fp8_src}") if i8 else
                                        f"fp8 dense, burst: {fp8_src}"),
@@ -946,7 +947,7 @@ def run_ours(args):
                                        "frac": fwd_tflops / DATASHEET_MMA_TFLOPS["int8" if i8 else "e4m3"]}},
             "roofline_prepare": {"kernel": "attnq_prepare (all passes)", "bound": "hbm", "achieved": prep_gbs,
                                  "peak": peaks["hbm"], "unit": "GB/s", "frac": prep_gbs / peaks["hbm"],
-                                 "traffic": ncu_traffic("attnq_prepare" + tag, prep_hash),
+                                 "traffic": ncu_traffic("attnq_prepare" + tag, prep_hash) if full_size else None,
                                  "bytes_per_launch": prep_bytes, "ms_per_launch": t_prep * 1e3},
             "err_vs_fp64": err_sample,
             "cpu_baseline": cpu,
