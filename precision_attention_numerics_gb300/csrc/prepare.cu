@@ -90,7 +90,7 @@ struct FlowCfg {
   static constexpr int NST = NST1 - NST1 % kGroups;
   static constexpr int WORDS = BF16 ? D / 2 : D;  // 32-bit input words per row
   static constexpr size_t SMEM = 1024 + size_t(NST) * SB + size_t(NBUF * kConsumerWarps) * WB + 16 * NST +
-                                 16 * NST + 4 * WORDS + 8 * (D / 2) + kConsumerWarps * 8 * (D / 2) +
+                                 16 * NST + 8 * WORDS + 8 * (D / 2) + kConsumerWarps * 8 * (D / 2) +
                                  4 * 4 * 2 * kGroups + 8 * 2 * kGroups;
   static_assert(NST >= kGroups && NST % kGroups == 0, "pipeline depth: whole stages per group");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -438,22 +438,37 @@ __device__ __forceinline__ void load_row(const uint8_t* stage, int r, const uint
   auto chunk = [&](int q) -> uint4 {
     const int box = q / 8, cq = q % 8;
     uint4 u = *reinterpret_cast<const uint4*>(rowp + box * (kTR * 128) + ((cq ^ r7) << 4));
-    if constexpr (FLIP) {
+    if constexpr (FLIP && !BF16) {
       const uint4 m = *reinterpret_cast<const uint4*>(smask + 4 * q);
       u.x ^= m.x; u.y ^= m.y; u.z ^= m.z; u.w ^= m.w;
     }
     return u;
+  };
+  // bf16 with the flip: the high element is (w ^ m) & 0xFFFF0000, one
+  // three-input logic op; the low one is (w << 16) + (m << 16), where adding
+  // 0 or 2^31 modulo 2^32 is the XOR of bit 31 (one shift-and-add).
+  auto mask = [&](int q, int lo) -> uint4 {
+    return *reinterpret_cast<const uint4*>(smask + (lo ? C::WORDS : 0) + 4 * q);
   };
   // chunk q holds elements PER*q ..; it pairs with chunk q + CH/2 (elements + D/2)
 #pragma unroll
   for (int q = 0; q < CH / 2; ++q) {
     const uint4 ua = chunk(q), ub = chunk(q + CH / 2);
     const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+    uint32_t ha[4] = {0u, 0u, 0u, 0u}, hb[4] = {0u, 0u, 0u, 0u}, la[4] = {0u, 0u, 0u, 0u}, lb[4] = {0u, 0u, 0u, 0u};
+    if constexpr (FLIP && BF16) {
+      const uint4 mha = mask(q, 0), mhb = mask(q + CH / 2, 0), mla = mask(q, 1), mlb = mask(q + CH / 2, 1);
+      ha[0] = mha.x; ha[1] = mha.y; ha[2] = mha.z; ha[3] = mha.w;
+      hb[0] = mhb.x; hb[1] = mhb.y; hb[2] = mhb.z; hb[3] = mhb.w;
+      la[0] = mla.x; la[1] = mla.y; la[2] = mla.z; la[3] = mla.w;
+      lb[0] = mlb.x; lb[1] = mlb.y; lb[2] = mlb.z; lb[3] = mlb.w;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if constexpr (BF16) {
-        P[PER * q + 2 * i] = pack2(__uint_as_float(wa[i] << 16), __uint_as_float(wb[i] << 16));
-        P[PER * q + 2 * i + 1] = pack2(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(wb[i] & 0xFFFF0000u));
+        P[PER * q + 2 * i] = pack2(__uint_as_float((wa[i] << 16) + la[i]), __uint_as_float((wb[i] << 16) + lb[i]));
+        P[PER * q + 2 * i + 1] =
+            pack2(__uint_as_float((wa[i] ^ ha[i]) & 0xFFFF0000u), __uint_as_float((wb[i] ^ hb[i]) & 0xFFFF0000u));
       } else {
         P[PER * q + i] = pack2(__uint_as_float(wa[i]), __uint_as_float(wb[i]));
       }
@@ -646,8 +661,9 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
   TileMeta* meta = reinterpret_cast<TileMeta*>(outb + size_t(C::NBUF * kConsumerWarps) * C::WB);
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + C::NST);
   uint64_t* empty = full + C::NST;
-  uint32_t* smask = reinterpret_cast<uint32_t*>(empty + C::NST);  // sign-bit mask per input word
-  uint64_t* pmask = reinterpret_cast<uint64_t*>(smask + C::WORDS);  // sign-bit masks of the pairs (x_j, x_{j+D/2})
+  // sign-bit mask per input word, then (bf16) the low element's sign moved to bit 31
+  uint32_t* smask = reinterpret_cast<uint32_t*>(empty + C::NST);
+  uint64_t* pmask = reinterpret_cast<uint64_t*>(smask + 2 * C::WORDS);  // sign-bit masks of the pairs (x_j, x_{j+D/2})
   uint64_t* nmu_all = pmask + D / 2;                               // per consumer warp: -mu as pairs [D/2]
   // per-tile scales: each group's four warp maxima of a tile, two slots by
   // tile parity, and the barriers (four arrivals) that publish them
@@ -673,6 +689,7 @@ __global__ void __launch_bounds__(kFlowThreads, 1)
       }
     }
     smask[i] = m;
+    smask[C::WORDS + i] = m << 16;
   }
   for (int j = threadIdx.x; j < D / 2; j += blockDim.x) {
     const uint64_t lo = (a.rotate && a.signs[j] < 0) ? 0x80000000ull : 0ull;
