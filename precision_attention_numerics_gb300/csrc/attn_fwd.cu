@@ -138,6 +138,17 @@ struct Unit {
   int t, b, g, h0, nact, nt;
 };
 
+// Unit index of round k for this CTA.  Units are ordered longest first and a
+// round hands one unit to each CTA; rounds alternate direction (CTA i takes
+// the i-th unit of an even round and the i-th from the end of an odd one), so
+// every CTA gets the same total number of key tiles to within one round's
+// spread, where a fixed stride would give the CTAs with low indices the longer
+// unit of every round.
+__device__ __forceinline__ int unit_of_round(int k) {
+  const int g = int(gridDim.x), i = int(blockIdx.x);
+  return k * g + ((k & 1) ? g - 1 - i : i);
+}
+
 template <int T>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
   const int per_t = p.B * p.Hkv * p.pairs;
@@ -217,7 +228,7 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
   bool ok = true;
   bool q_issued = false;
   int q_last = 0;
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+  for (int k_r = 0, u = unit_of_round(0); u < p.n_units && ok; u = unit_of_round(++k_r), ++uc) {
     const Unit un = decode_unit<T>(p, u);
     const int qb = uc % C::QBUF;
     if (!wait_or_abort(br.q_empty + qb, ((uc / C::QBUF) & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
@@ -352,7 +363,7 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
     return true;
   };
 
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x, ++uc) {
+  for (int k_r = 0, u = unit_of_round(0); u < p.n_units && ok; u = unit_of_round(++k_r), ++uc) {
     const Unit un = decode_unit<T>(p, u);
     const int qb = uc % C::QBUF;
     if (!vote_wait(br.q_full + qb, (uc / C::QBUF) & 1, p, abort_flag)) { ok = false; break; }
@@ -435,7 +446,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
     return warp_wait(br.o_done + 2 * w + (n & 1u), (n >> 1) & 1u, p, abort_flag);
   };
   bool ok = true;
-  for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+  for (int k_r = 0, u = unit_of_round(0); u < p.n_units && ok; u = unit_of_round(++k_r)) {
     const Unit un = decode_unit<T>(p, u);
     if (w >= un.nact) continue;  // sits the unit out: no arrival on o_free (its warps would not be in step)
     const int h = un.h0 + w;
