@@ -12,7 +12,8 @@ Prints one JSON line (rank 0).  `value` is algorithmic attention TFLOP/s
 step; `e2e` repeats the measurement through the C ABI's host-buffer pipeline
 (attnq_attention_host): every step copies its bf16 inputs in from pinned host
 memory and its output back inside the timed region, the copies of
-neighbouring steps overlapping each step's kernels.  Under torchrun every rank runs its own independent replica
+neighbouring steps overlapping each step's kernels (its own SM-clock sample
+in `e2e.clocks`).  Under torchrun every rank runs its own independent replica
 (weak scaling, no collective on the data path).
 
 The attention roofline divides by this GPU's dense FP8 GEMM rate, measured
@@ -842,6 +843,7 @@ def run_ours(args):
     # its Q, K, V in from pinned host memory and its O back out; the copies of
     # step s+1's inputs and step s-1's output overlap step s's kernels
     e2e_elapsed = float("nan")
+    e2e_clocks = None
     if not args.no_e2e:
         del bufs  # the pipeline keeps its own device buffers in its workspace
         compute, copy_in, copy_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -856,10 +858,12 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(compute)
-        e2e_run(args.steps)
-        s1.record(compute)
-        torch.cuda.synchronize()
+        with ClockSampler(local) as e2e_clk:
+            s0.record(compute)
+            e2e_run(args.steps)
+            s1.record(compute)
+            torch.cuda.synchronize()
+        e2e_clocks = e2e_clk.summary()
         e2e_elapsed = s0.elapsed_time(s1) / 1e3
         st = aq.attnq_device_status(compute.cuda_stream)
         if st != 0:
@@ -953,7 +957,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": None if args.no_e2e else {
                 "value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_elapsed / args.steps * 1e3},
+                "ms_per_step": e2e_elapsed / args.steps * 1e3, "clocks": e2e_clocks},
             "clocks": clocks,
             "gpu_launches": args.steps * launches_per_step(flags),
         }
