@@ -19,7 +19,8 @@
 // Work unit: one 128-row query tile of two query heads that share a KV head
 // (GQA); both use the same K/V tiles and the same KV range.  A persistent
 // grid walks the units longest-first (query tiles nearest the end of the
-// sequence have the most KV tiles).
+// sequence have the most KV tiles), one unit per CTA per round, in rounds of
+// alternating direction so that every CTA gets the same number of KV tiles.
 //
 // CTA = 384 threads:
 //   warps 0-3  softmax warpgroup 0 (query head h0), TMEM lanes 0..127 = rows
@@ -52,9 +53,8 @@
 // on barrier n % 2), so the softmax waits only for the products it needs:
 // product n-2 before reusing its P buffer, n-1 before a rescale.  "P ready"
 // alternates the same way, because a warpgroup's warps drift apart by up to
-// one tile.
-// so S_w(k+1) and the P.V products run on the tensor core while the softmax
-// warps compute, and the softmax never waits for its own S(k+1) MMA.
+// one tile.  S_w(k+1) and the P.V products thus run on the tensor core while
+// the softmax warps compute.
 //
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // DEV_TIMEOUT, every role leaves its loop, outstanding TMA loads and MMAs are
