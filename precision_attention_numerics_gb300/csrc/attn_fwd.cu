@@ -85,6 +85,7 @@ constexpr uint64_t kDrainNs = 1000000000ull;
 
 struct Params {
   int B, Hq, Hkv, N, G, pairs, n_qt, n_units;
+  int paired;  // 1: the mirrored-pair schedule (unit_at), 0: alternating rounds of single units
   int causal, reverse;
   float S, log2S;
   const float* q_ds;
@@ -138,15 +139,30 @@ struct Unit {
   int t, b, g, h0, nact, nt;
 };
 
-// Unit index of round k for this CTA.  Units are ordered longest first and a
-// round hands one unit to each CTA; rounds alternate direction (CTA i takes
-// the i-th unit of an even round and the i-th from the end of an odd one), so
-// every CTA gets the same total number of key tiles to within one round's
-// spread, where a fixed stride would give the CTAs with low indices the longer
-// unit of every round.
-__device__ __forceinline__ int unit_of_round(int k) {
+// Unit index (in decode_unit's numbering) of this CTA's k-th unit; p.n_units
+// once the CTA has none left.  Two schedules, both handing the same KV-tile
+// total to every CTA:
+// * alternating rounds: units ordered longest first, one per CTA per round,
+//   rounds of alternating direction (CTA i takes the i-th unit of an even
+//   round and the i-th from the end of an odd one; a fixed stride would give
+//   the CTAs with low indices the longer unit of every round);
+// * mirrored pairs (causal, an even number of query tiles, many rounds): an
+//   item is query tile n_qt-1-s followed by its mirror s of the same heads,
+//   n_qt + 1 key tiles of 128 keys together, and items go one per CTA per
+//   round in (batch, KV group)-major order.  The CTAs of a round then share
+//   the K/V tiles of one or two KV groups, which stay in L2, where the
+//   longest-first order keeps every group's K and V in use at once and reads
+//   them from DRAM several times over.
+__device__ __forceinline__ int unit_at(const Params& p, int k) {
   const int g = int(gridDim.x), i = int(blockIdx.x);
-  return k * g + ((k & 1) ? g - 1 - i : i);
+  if (!p.paired) return k * g + ((k & 1) ? g - 1 - i : i);
+  const int half = p.n_qt / 2, per_grp = half * p.pairs;
+  const int j = (k >> 1) * g + i;  // item
+  if (j >= p.B * p.Hkv * per_grp) return p.n_units;
+  const int grp = j / per_grp, rem = j % per_grp;  // grp = b * Hkv + kv group
+  const int s = rem / p.pairs, pr = rem % p.pairs;
+  const int t = (k & 1) ? s : p.n_qt - 1 - s;
+  return (p.n_qt - 1 - t) * (p.B * p.Hkv * p.pairs) + grp * p.pairs + pr;
 }
 
 template <int T>
@@ -228,7 +244,7 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
   bool ok = true;
   bool q_issued = false;
   int q_last = 0;
-  for (int k_r = 0, u = unit_of_round(0); u < p.n_units && ok; u = unit_of_round(++k_r), ++uc) {
+  for (int k_r = 0, u = unit_at(p, 0); u < p.n_units && ok; u = unit_at(p, ++k_r), ++uc) {
     const Unit un = decode_unit<T>(p, u);
     const int qb = uc % C::QBUF;
     if (!wait_or_abort(br.q_empty + qb, ((uc / C::QBUF) & 1) ^ 1, p.wait_ns, abort_flag)) { ok = false; break; }
@@ -363,7 +379,7 @@ __device__ __forceinline__ void mma_issuer(const Params& p, int w, uint32_t tmem
     return true;
   };
 
-  for (int k_r = 0, u = unit_of_round(0); u < p.n_units && ok; u = unit_of_round(++k_r), ++uc) {
+  for (int k_r = 0, u = unit_at(p, 0); u < p.n_units && ok; u = unit_at(p, ++k_r), ++uc) {
     const Unit un = decode_unit<T>(p, u);
     const int qb = uc % C::QBUF;
     if (!vote_wait(br.q_full + qb, (uc / C::QBUF) & 1, p, abort_flag)) { ok = false; break; }
@@ -446,7 +462,7 @@ __device__ __forceinline__ void softmax_wg(const Params& p, int w, uint32_t tmem
     return warp_wait(br.o_done + 2 * w + (n & 1u), (n >> 1) & 1u, p, abort_flag);
   };
   bool ok = true;
-  for (int k_r = 0, u = unit_of_round(0); u < p.n_units && ok; u = unit_of_round(++k_r)) {
+  for (int k_r = 0, u = unit_at(p, 0); u < p.n_units && ok; u = unit_at(p, ++k_r)) {
     const Unit un = decode_unit<T>(p, u);
     if (w >= un.nact) continue;  // sits the unit out: no arrival on o_free (its warps would not be in step)
     const int h = un.h0 + w;
@@ -826,6 +842,12 @@ cudaError_t run(const FwdArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < a.num_sms ? p.n_units : a.num_sms;
+  // mirrored pairs where every CTA gets the same number of items to within
+  // 1 % (the last round nearly full) over at least four rounds
+  {
+    const int64_t items = int64_t(p.n_units) / 2, rounds = (items + grid - 1) / grid;
+    p.paired = (a.causal && p.n_qt % 2 == 0 && items >= 4 * int64_t(grid) && 100 * rounds * grid <= 101 * items) ? 1 : 0;
+  }
   kern<<<grid, kThreads, C::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -13,7 +13,9 @@ against the oracle:
 * the long-context workload at full size in the configuration bench.py times
   (B=2, Hq=32, Hkv=8, N=32768, d=128, rotation + centring, reverse, S=256,
   bf16 output): every E4M3 operand byte, descale and mean-key value, and the
-  outputs of sampled rows of sampled heads.
+  outputs of sampled rows of sampled heads;
+* a shape on the attention kernel's mirrored-pair schedule with an odd GQA
+  group, 64-key tiles, forward order and ragged N (sampled rows).
 """
 import numpy as np
 import pytest
@@ -121,5 +123,36 @@ def test_long_context_full_size_sampled():
     rows = np.array([0, 1, 127, 128, 4095, 16383, 16384, 24577, 32640, 32767], dtype=np.int32)
     bh = [0, 5, 31, 32, 63]
     emu, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, 1, True, T, bh_list=bh, rows=rows)
+    got = o_to_numpy(O).reshape(B * Hq, N, d)[bh][:, rows]
+    assert rel_f(got, oracle_bf16(emu)).max() <= REL_F_TOL
+
+
+def test_mirrored_pair_schedule_sampled():
+    """A shape whose unit count puts the attention kernel on its mirrored-pair
+    schedule on a 152-SM GPU (causal, 380 query tiles: 760 items of two
+    mirrored query tiles, five full rounds), with the cases that schedule must
+    still get right: a GQA group of three query heads (its second pair has one
+    head), 64-key tiles, forward KV order, ragged N.  Every operand byte
+    against the oracle, and the outputs of sampled rows (both ends of the
+    sequence, the mirrored tiles' edges, the ragged tail)."""
+    import precision_attention_numerics_gb300 as aq
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, oracle_bf16, rel_f
+    B, Hq, Hkv, d, T = 1, 6, 2, 64, 64
+    N = 380 * 128 - 37
+    q, k, v = synth.long_context_inputs(5101, B, Hq, Hkv, N, d)
+    signs = synth.hadamard_signs(5102, d)
+    flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    O, _, st = gpu_fwd(desc, bufs, 448.0, 0, True, T, out_dtype=torch.bfloat16, count=False)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs)
+    assert torch.equal(bufs.q8.cpu(), torch.from_numpy(prep["q8"]))
+    assert torch.equal(bufs.k8.cpu(), torch.from_numpy(prep["k8"]))
+    v8 = bufs.v8[..., :N].transpose(-1, -2).contiguous().cpu()
+    assert torch.equal(v8, torch.from_numpy(prep["v8"]))
+    rows = np.array([0, 127, 128, 255, 24191, 24192, 48255, 48256, 48500, N - 1], dtype=np.int32)
+    bh = [0, 2, 3, 5]
+    emu, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 448.0, 0, True, T, bh_list=bh, rows=rows)
     got = o_to_numpy(O).reshape(B * Hq, N, d)[bh][:, rows]
     assert rel_f(got, oracle_bf16(emu)).max() <= REL_F_TOL
