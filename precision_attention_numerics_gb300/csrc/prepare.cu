@@ -55,6 +55,11 @@ namespace {
 
 constexpr int kTR = 128;           // rows per tile = tokens per mean-key chunk
 constexpr int kTilesPerItem = 16;  // tiles per claimed item
+// The last kTailEntries entries of the list (cast entries: the list ends with
+// the casts of the slices whose amax came last) are claimed in items of
+// kTilesPerItem / kTailSplit tiles, so the CTAs run out of work within a few
+// tiles of one another instead of within one 16-tile item.
+constexpr uint32_t kTailEntries = 7, kTailSplit = 4;
 constexpr int kGroups = 2;         // consumer groups (4 warps, one row per thread)
 constexpr int kConsumerWarps = 4 * kGroups;
 constexpr int kFlowThreads = 128 * (kGroups + 1);  // consumer warpgroups + a warpgroup whose first warp is the producer
@@ -300,7 +305,10 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
                          uint64_t* full, uint64_t* empty) {
   using C = FlowCfg<D, BF16, I8>;
   const PrepareArgs& a = f.a;
-  const uint32_t total = a.ctl[CTL_ENTRIES] * uint32_t(f.items_per_slice);
+  const uint32_t ips = uint32_t(f.items_per_slice), n_ent = a.ctl[CTL_ENTRIES];
+  const uint32_t tail_ent = n_ent < kTailEntries ? n_ent : kTailEntries;
+  const uint32_t t_small = (n_ent - tail_ent) * ips;  // tickets before the small items
+  const uint32_t total = t_small + tail_ent * ips * kTailSplit;
   // A slice's data is read again by a later pass (A after M, C after A):
   // keep it in L2 until the C pass reads it for the last time.
   const uint64_t keep = l2_evict_last_policy(), last_use = l2_evict_first_policy();
@@ -315,16 +323,19 @@ __device__ void producer(const Flow& f, const CUtensorMap* const* in_maps, uint8
     if (aborted(a)) { ok = false; break; }
     if (t >= total) break;
     uint32_t t_next = 0;
-    const uint32_t ent = a.entries[t / uint32_t(f.items_per_slice)];
-    const uint32_t item = t % uint32_t(f.items_per_slice);
+    const bool small = t >= t_small;
+    const uint32_t ent = a.entries[small ? n_ent - tail_ent + (t - t_small) / (ips * kTailSplit) : t / ips];
+    const uint32_t item = small ? (t - t_small) % (ips * kTailSplit) : t % ips;
+    const int tpi = small ? kTilesPerItem / int(kTailSplit) : kTilesPerItem;
     const uint32_t kind = ent >> 30, s = ent & 0x3FFFFFFFu;
     const SliceRef r = slice_ref(a, int(s));
     const CUtensorMap* map = in_maps[r.tensor];
-    const int row_begin = int(item) * kTR * kTilesPerItem;
-    // the M and A passes read only the first P tokens: their later items are empty
+    const int row_begin = int(item) * kTR * tpi;
+    // the M and A passes read only the first P tokens: their later items are
+    // empty; so are the small items past a slice's last tile
     const int lim = (PREFIX && kind != KIND_C) ? a.P : a.N;
-    const int nt = min(kTilesPerItem, (lim - row_begin + kTR - 1) / kTR);
-    if (PREFIX && nt <= 0) {
+    const int nt = min(tpi, (lim - row_begin + kTR - 1) / kTR);
+    if (nt <= 0) {
       t = atomicAdd(a.ctl + CTL_TICKET, 1u);
       continue;
     }
