@@ -224,7 +224,10 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
  * within a few ulp of a rounding boundary.  A factor c below the smallest
  * normal float (FLT_MIN) is raised to FLT_MIN: every logit is then below
  * 2^-100 in magnitude either way (|s_j| < 2^25) and every P is 1 in fp32, so no result
- * changes, and masked keys keep P * S = 0.  With ATTNQ_TILE_SCALES, dq is row i's query tile's and dk
+ * changes, and masked keys keep P * S = 0.  A factor above the largest
+ * float (descale products near 1e39 and beyond: logits past the fp32 range)
+ * makes c infinite, as in the plain two-step evaluation: masked keys still
+ * give P * S = 0, and an unmasked score of exactly 0 gives NaN.  With ATTNQ_TILE_SCALES, dq is row i's query tile's and dk
  * key j's tile's descale (kv_tile divides the scale tile, so c is constant
  * within a KV tile).  desc: shape and flags of the attnq_prepare call that made
  * the operands (ATTNQ_VT_LAYOUT is required; in_dtype is ignored).
