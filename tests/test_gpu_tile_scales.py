@@ -84,3 +84,34 @@ def test_tile_instance_with_equal_tile_scales_equals_slice_instance(i8, T):
     O2, _, st = gpu_fwd(tdesc, bufs, 256.0, 1, True, T, out_dtype=torch.float32, count=False)
     assert st == 0
     assert torch.equal(O1, O2)
+
+
+def test_tile_scales_long_context_full_size_sampled():
+    """The long-context workload at full size with per-tile Q/K scales (the
+    shape runs the attention kernel's mirrored-pair schedule): every code and
+    descale against the oracle, and sampled output rows within the forward
+    tolerance."""
+    import torch
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, oracle_bf16, rel_f
+    wl = synth.WORKLOADS["long_context"]
+    B, Hq, Hkv, N, d, T = wl["B"], wl["Hq"], wl["Hkv"], wl["N"], wl["d"], wl["kv_tile"]
+    q, k, v = synth.long_context_inputs(5200, B, Hq, Hkv, N, d)
+    signs = synth.hadamard_signs(17, d)
+    flags = 3 | TILE
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    O, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, T, out_dtype=torch.bfloat16, count=False)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs)
+    assert torch.equal(bufs.q8.cpu(), torch.from_numpy(prep["q8"]))
+    assert torch.equal(bufs.k8.cpu(), torch.from_numpy(prep["k8"]))
+    v8 = bufs.v8[..., :N].transpose(-1, -2).contiguous().cpu()
+    assert torch.equal(v8, torch.from_numpy(prep["v8"]))
+    for key, t in (("q_descale", bufs.scales.q_descale), ("k_descale", bufs.scales.k_descale),
+                   ("v_descale", bufs.scales.v_descale), ("k_mean", bufs.scales.k_mean)):
+        assert np.array_equal(t.cpu().numpy().view(np.uint32), prep[key].view(np.uint32)), key
+    rows = np.array([0, 1, 127, 128, 4095, 16383, 16384, 24577, 32640, 32767], dtype=np.int32)
+    bh = [0, 5, 31, 32, 63]
+    emu, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, 1, True, T, bh_list=bh, rows=rows)
+    got = o_to_numpy(O).reshape(B * Hq, N, d)[bh][:, rows]
+    assert rel_f(got, oracle_bf16(emu)).max() <= REL_F_TOL
