@@ -16,6 +16,10 @@ neighbouring steps overlapping each step's kernels (its own SM-clock sample
 in `e2e.clocks`).  Under torchrun every rank runs its own independent replica
 (weak scaling, no collective on the data path).
 
+Each kernel's roofline object gives its mean per-launch time over the timed
+steps (CUDA events on its stream) with the median and the best beside it;
+`device` names the GPU (CUDA device properties).
+
 The attention roofline divides by this GPU's dense FP8 GEMM rate, measured
 in the same run after the timed region (cuBLASLt E4M3 GEMM at 8192^3 through
 torch._scaled_mm, best of 10: the burst figure, as the timed region is well
@@ -79,6 +83,15 @@ def prepare_bytes(B, Hq, Hkv, N, d, in_bytes=2, qk_code_bytes=1):
 # Dense tensor peaks from the datasheet, TFLOP/s: FP8 for the E4M3 step; for
 # INT8-QK half the flops run on the bf16 path, so 1 / (0.5 / 2250 + 0.5 / 4500).
 DATASHEET_MMA_TFLOPS = {"e4m3": 4500.0, "int8": 3000.0}
+
+
+def device_info(dev) -> dict:
+    """The GPU the line was measured on, from the CUDA device properties."""
+    import torch
+    pr = torch.cuda.get_device_properties(dev)
+    l2 = getattr(pr, "L2_cache_size", None)
+    return {"name": pr.name, "sm_count": pr.multi_processor_count, "cc": f"{pr.major}.{pr.minor}",
+            "l2_mb": None if l2 is None else round(l2 / 2**20, 1), "hbm_gib": round(pr.total_memory / 2**30, 1)}
 
 
 def load_peaks():
@@ -832,8 +845,10 @@ def run_ours(args):
         torch.cuda.synchronize()
     clocks = clk.summary()
     elapsed = start.elapsed_time(end) / 1e3
-    t_prep = sum(e0.elapsed_time(e1) for e0, e1, _ in ev) / args.steps / 1e3
-    t_fwd = sum(e1.elapsed_time(e2) for _, e1, e2 in ev) / args.steps / 1e3
+    prep_ms = sorted(e0.elapsed_time(e1) for e0, e1, _ in ev)
+    fwd_ms = sorted(e1.elapsed_time(e2) for _, e1, e2 in ev)
+    t_prep = sum(prep_ms) / args.steps / 1e3
+    t_fwd = sum(fwd_ms) / args.steps / 1e3
     st = aq.attnq_device_status()
     if st != 0:
         raise RuntimeError(f"device status {aq.STATUS.get(st, st)} in the timed region")
@@ -946,19 +961,22 @@ def run_ours(args):
                                         f"the bf16 path, P V on fp8; fp8 {fp8_src}") if i8 else
                                        f"fp8 dense, burst: {fp8_src}"),
                          "flops_per_launch": flops_step, "ms_per_launch": t_fwd * 1e3,
+                         "ms_median": statistics.median(fwd_ms), "ms_best": fwd_ms[0],
                          # the dense datasheet figure, for context (GB300: 4.5 PFLOP/s FP8, 2.25 bf16)
                          "datasheet": {"peak": DATASHEET_MMA_TFLOPS["int8" if i8 else "e4m3"],
                                        "frac": fwd_tflops / DATASHEET_MMA_TFLOPS["int8" if i8 else "e4m3"]}},
             "roofline_prepare": {"kernel": "attnq_prepare (all passes)", "bound": "hbm", "achieved": prep_gbs,
                                  "peak": peaks["hbm"], "unit": "GB/s", "frac": prep_gbs / peaks["hbm"],
                                  "traffic": ncu_traffic("attnq_prepare" + tag, prep_hash) if full_size else None,
-                                 "bytes_per_launch": prep_bytes, "ms_per_launch": t_prep * 1e3},
+                                 "bytes_per_launch": prep_bytes, "ms_per_launch": t_prep * 1e3,
+                                 "ms_median": statistics.median(prep_ms), "ms_best": prep_ms[0]},
             "err_vs_fp64": err_sample,
             "cpu_baseline": cpu,
             "e2e": None if args.no_e2e else {
                 "value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_elapsed / args.steps * 1e3, "clocks": e2e_clocks},
             "clocks": clocks,
+            "device": device_info(dev),
             "gpu_launches": args.steps * launches_per_step(flags),
         }
     if dist is not None:
