@@ -87,3 +87,18 @@ def test_descriptor_layout_matches_the_header(aq, tmp_path):
     want = [C.sizeof(binding._Desc), binding._Desc.signs.offset, binding._Desc.stat_len.offset,
             C.sizeof(binding._Scales)]
     assert got == want
+
+
+def test_missing_library_fails_loudly(aq, tmp_path):
+    """Without the compiled library every call raises: there is no other path."""
+    from precision_attention_numerics_gb300 import binding
+    saved_path, saved_lib = binding._LIB_PATH, binding._lib
+    try:
+        binding._LIB_PATH = str(tmp_path / "libattnq.so")
+        binding._lib = None
+        with pytest.raises(RuntimeError, match="is missing"):
+            binding.load_library()
+        with pytest.raises(RuntimeError, match="is missing"):
+            aq.attnq_version()
+    finally:
+        binding._LIB_PATH, binding._lib = saved_path, saved_lib
