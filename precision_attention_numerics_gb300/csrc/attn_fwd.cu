@@ -222,7 +222,7 @@ __device__ __forceinline__ void raise_abort(const Params& p, volatile int* abort
 
 // Warp-uniform wait.  Fast path: every lane tests the barrier and the warp
 // votes (no divergence, no broadcast); otherwise lane 0 waits with the bound
-// and the verdict is broadcast.
+// and the result is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const Params& p,
                                           volatile int* abort_flag) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
@@ -303,7 +303,7 @@ __device__ __forceinline__ void producer(const Params& p, const CUtensorMap* tq,
 }
 
 // Wait for a converged warp: every lane waits (they sleep in try_wait) and
-// the verdict is voted, so the warp leaves converged.
+// the result is voted, so the warp leaves converged.
 __device__ __forceinline__ bool vote_wait(uint64_t* bar, uint32_t parity, const Params& p, volatile int* abort_flag) {
   const bool ok = wait_or_abort(bar, parity, p.wait_ns, abort_flag);
   return __all_sync(0xffffffffu, ok);
