@@ -232,7 +232,12 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
  * within a KV tile).  desc: shape and flags of the attnq_prepare call that made
  * the operands (ATTNQ_VT_LAYOUT is required; in_dtype is ignored).
  * q8, k8, v8, scales: DEVICE, as written by attnq_prepare.  S: finite, in
- * (0, 448].  kv_order: ATTNQ_KV_FORWARD or ATTNQ_KV_REVERSE.  kv_tile: 64 or
+ * (0, 448], and not within a relative 2^-20 of a point where E4M3 rounding
+ * changes (S = 100, halfway between the codes 96 and 104, is refused with
+ * ATTNQ_EINVAL): the row maximum's P * S, exactly S in the two-step form,
+ * comes out of the single exp2 within a few 2^-24 of S and must round as S
+ * does.  The pages' 1, 256 and 448 are E4M3 values, as is every power of two
+ * in range.  kv_order: ATTNQ_KV_FORWARD or ATTNQ_KV_REVERSE.  kv_tile: 64 or
  * 128.  O: DEVICE [B,Hq,N,d] of out_dtype (ATTNQ_F32 or ATTNQ_BF16, RNE).
  * underflow_opt: NULL, or DEVICE uint64 [B*Hq*2] that the call ADDS to:
  * [2*bh] counts in-mask keys j >= k_sink of KV tile 0 whose P*S > 0 was cast
@@ -289,8 +294,9 @@ attnq_status attnq_ref_attention(const attnq_desc* desc, const void* Q, const vo
  * required; desc->flags is ignored (the conditions use E4M3 codes and one
  * scale per (batch, head)); desc->stat_len applies.  workspace: DEVICE, 256-byte aligned, at
  * least attnq_harm_workspace(desc) bytes (it holds the fp64 reference, the
- * fp32 output, the E4M3 operands and the prepare workspace).  Errors of any
- * step are returned as that step returns them.
+ * fp32 output, the E4M3 operands and the prepare workspace).  S: as for
+ * attnq_fwd (checked before any launch).  Errors of any other step are
+ * returned as that step returns them.
  */
 size_t attnq_harm_workspace(const attnq_desc* desc);
 attnq_status attnq_harm_report(const attnq_desc* desc, const void* Q, const void* K, const void* V, float S,

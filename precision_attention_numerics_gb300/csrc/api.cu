@@ -53,6 +53,28 @@ attnq_status device_setup(int* dev_out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Value of x > 0 rounded to the nearest E4M3 value, ties to even, saturating
+// at 448: normal binades 2^e (e >= -6) hold 8 values 2^(e-3) apart, below
+// 2^-6 the step is 2^-9.
+double e4m3_round_host(double x) {
+  if (x >= 448.0) return 448.0;
+  const int e = int(std::floor(std::log2(x)));
+  const double q = std::ldexp(1.0, e < -6 ? -9 : e - 3);
+  return std::nearbyint(x / q) * q;  // default rounding mode: half to even
+}
+
+// A P-cast scale is usable by attnq_fwd unless it lies within a relative 2^-20
+// of a point where the E4M3 rounding of P * S changes: the kernel forms P * S
+// in one exp2 of fma(s, c, log2 S - m'), so the row maximum's P * S, exactly S
+// in the two-step form, comes out S (1 +- a few 2^-24) and would round to
+// either neighbour of such a point (S = 100, halfway between 96 and 104, is
+// one).
+bool pcast_scale_ok(float S) {
+  if (!(std::isfinite(S) && S > 0.0f && S <= 448.0f)) return false;
+  const double s = double(S), r = std::ldexp(1.0, -20);
+  return e4m3_round_host(s * (1.0 - r)) == e4m3_round_host(s * (1.0 + r));
+}
+
 attnq_status check_desc(const attnq_desc* d) {
   if (!d) return ATTNQ_EINVAL;
   if (d->B <= 0 || d->Hq <= 0 || d->Hkv <= 0 || d->N <= 0 || d->d <= 0) return ATTNQ_EINVAL;
@@ -326,7 +348,7 @@ attnq_status attnq_fwd(const attnq_desc* desc, const uint8_t* q8, const uint8_t*
   if (!q8 || !k8 || !v8 || !scales || !scales->q_descale || !scales->k_descale || !scales->v_descale || !O)
     return ATTNQ_EINVAL;
   if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(O)) return ATTNQ_EINVAL;
-  if (!(std::isfinite(S) && S > 0.0f && S <= 448.0f)) return ATTNQ_EINVAL;
+  if (!pcast_scale_ok(S)) return ATTNQ_EINVAL;
   if (kv_order != ATTNQ_KV_FORWARD && kv_order != ATTNQ_KV_REVERSE) return ATTNQ_EINVAL;
   if (causal != 0 && causal != 1) return ATTNQ_EINVAL;
   if (out_dtype != ATTNQ_F32 && out_dtype != ATTNQ_BF16) return ATTNQ_EINVAL;
@@ -431,6 +453,7 @@ attnq_status attnq_harm_report(const attnq_desc* desc, const void* Q, const void
   attnq_status st = check_desc(desc);
   if (st != ATTNQ_OK) return st;
   if (!desc->signs || !err_out || !workspace) return ATTNQ_EINVAL;
+  if (!pcast_scale_ok(S)) return ATTNQ_EINVAL;
   const HarmLayout L = harm_layout(desc);
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTNQ_EINVAL;
   char* w = static_cast<char*>(workspace);
@@ -481,7 +504,7 @@ attnq_status attnq_attention_host(const attnq_desc* desc, int32_t n_steps, const
   // what attnq_prepare and attnq_fwd would refuse, refused before any work
   if (!(desc->flags & ATTNQ_VT_LAYOUT)) return ATTNQ_EUNSUPPORTED;
   if ((desc->flags & ATTNQ_ROTATE) && !desc->signs) return ATTNQ_EINVAL;
-  if (!(std::isfinite(S) && S > 0.0f && S <= 448.0f)) return ATTNQ_EINVAL;
+  if (!pcast_scale_ok(S)) return ATTNQ_EINVAL;
   if (kv_order != ATTNQ_KV_FORWARD && kv_order != ATTNQ_KV_REVERSE) return ATTNQ_EINVAL;
   if (causal != 0 && causal != 1) return ATTNQ_EINVAL;
   if (kv_tile != 64 && kv_tile != 128) return ATTNQ_EUNSUPPORTED;

@@ -60,6 +60,25 @@ def test_argument_checks_before_any_cuda_call(aq):
         assert rc == code, (desc, rc)
 
 
+def test_pcast_scales_on_an_e4m3_rounding_point_are_refused(aq):
+    """attnq_fwd forms P * S in one exp2, so S must round as P * S at P = 1
+    does: S within 2^-20 of an E4M3 rounding point (100 is halfway between 96
+    and 104) is refused before any CUDA call; E4M3 values and S clear of such
+    points pass it and stop at the next check (a KV tile of 96: unsupported)."""
+    L = aq.load_library()
+    d = aq.AttnqDesc(1, 1, 1, 16, 64, flags=aq.ATTNQ_VT_LAYOUT)._c()
+    fake = C.c_void_p(4096)
+    scales = aq.binding._Scales(4096, 4096, 4096, None)
+
+    def rc(S):
+        return L.attnq_fwd(C.byref(d), fake, fake, fake, C.byref(scales), C.c_float(S), 0, 1, 96, fake, 0, None, 4,
+                           None)
+    for S in (100.0, 50.0, 200.0, 25.0, 100.0 * (1 + 2.0 ** -22), 0.0, 449.0, float("nan")):
+        assert rc(S) == 1, S  # ATTNQ_EINVAL
+    for S in (1.0, 256.0, 448.0, 96.0, 101.0, 0.5, 3.0, 2.0 ** -8):
+        assert rc(S) == 2, S  # past the S check: ATTNQ_EUNSUPPORTED for the tile
+
+
 def test_workspace_size_grows_with_centring(aq):
     d0 = aq.AttnqDesc(2, 32, 8, 32768, 128, flags=aq.ATTNQ_VT_LAYOUT)
     d1 = aq.AttnqDesc(2, 32, 8, 32768, 128, flags=aq.ATTNQ_VT_LAYOUT | aq.ATTNQ_CENTER_K)

@@ -119,8 +119,10 @@ def test_rejects_bad_arguments():
     q, k, v = synth.sink_inputs(98, 1, 1, 64, 64, delta=1.0)
     desc, bufs, _ = gpu_prepare(q, k, v, 0, None)
     O = torch.empty((1, 1, 64, 64), device="cuda")
-    for kwargs, code in ((dict(S=0.0), 1), (dict(S=500.0), 1), (dict(S=float("nan")), 1), (dict(kv_tile=96), 2),
-                         (dict(kv_order=3), 1)):
+    # S = 100 lies halfway between the E4M3 values 96 and 104: refused (the
+    # single-exp2 P * S of the row maximum would round either way)
+    for kwargs, code in ((dict(S=0.0), 1), (dict(S=500.0), 1), (dict(S=float("nan")), 1), (dict(S=100.0), 1),
+                         (dict(kv_tile=96), 2), (dict(kv_order=3), 1)):
         args = dict(S=256.0, kv_order=0, causal=True, kv_tile=64)
         args.update(kwargs)
         with pytest.raises(aq.AttnqError) as e:

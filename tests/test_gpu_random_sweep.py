@@ -1,0 +1,72 @@
+"""A seeded sweep of random option combinations, each run end to end on the
+GPU and checked against the oracle: shapes (B, GQA group, ragged N, d), KV
+tile, order, causal or not, P-cast scale, rotation and centring, input and
+output types, per-tile scales and causal-prefix statistics, INT8 Q/K codes.
+The structured tests cover each option on its own; this covers them mixed.
+Bars: every operand byte and descale equal to the oracle's (INT8 codes by
+value), outputs within the forward tolerance of the oracle's emulation.
+
+The P-cast scales are the pages' three plus E4M3 values that are not powers
+of two and a value clear of any E4M3 rounding point (attnq_fwd refuses S on
+such a point).  N starts at 256: a P * S within an ulp or two of an E4M3
+rounding point can take the other code under the hardware exp2 (its rare,
+documented difference from the oracle's exact exp2), and in a head of a few
+dozen keys per row one such code moves the head's relative error by about
+2e-3 by itself (N = 67 gave 2.4e-3; perturbing the oracle's exp2 by 2^-22
+reproduces it to the last digit); over hundreds of keys per row it does not."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+ROT, CEN, TILE, I8 = 1, 2, 8, 16
+
+
+def _configs(n, seed=7301):
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        Hkv = rng.choice([1, 2, 3])
+        c = dict(B=rng.choice([1, 2]), Hkv=Hkv, Hq=Hkv * rng.choice([1, 2, 3, 4, 5]), N=rng.randint(256, 1200),
+                 d=rng.choice([64, 128]), T=rng.choice([64, 128]), order=rng.choice([0, 1]),
+                 causal=rng.random() < 0.8, S=rng.choice([1.0, 256.0, 448.0, 96.0, 320.0, 101.0]),
+                 flags=rng.choice([0, ROT, CEN, ROT | CEN]) | (TILE if rng.random() < 0.25 else 0)
+                 | (I8 if rng.random() < 0.25 else 0),
+                 f32_in=rng.random() < 0.3, bf16_out=rng.random() < 0.5, seed=8000 + i)
+        c["stat_len"] = rng.randint(1, c["N"]) if (rng.random() < 0.25 and not c["flags"] & TILE) else 0
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("cfg", _configs(32), ids=lambda c: f"s{c['seed']}")
+def test_random_option_mix(cfg):
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, oracle_bf16, prepared_to_numpy, rel_f
+    B, Hq, Hkv, N, d, T = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"], cfg["T"]
+    q, k, v = synth.qkv_normal(cfg["seed"], B, Hq, Hkv, N, d)
+    if not cfg["f32_in"]:
+        q, k, v = synth.to_bf16_bits(q), synth.to_bf16_bits(k), synth.to_bf16_bits(v)
+    flags = cfg["flags"]
+    signs = synth.hadamard_signs(cfg["seed"] + 1, d) if flags & ROT else None
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs, stat_len=cfg["stat_len"])
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs, stat_len=cfg["stat_len"])
+    got = prepared_to_numpy(desc, bufs)
+    for key in ("q8", "k8", "v8"):
+        assert np.array_equal(got[key], prep[key]), key
+    for key in ("q_descale", "k_descale", "v_descale"):
+        assert np.array_equal(got[key].view(np.uint32), prep[key].view(np.uint32)), key
+    out_dtype = torch.bfloat16 if cfg["bf16_out"] else torch.float32
+    O, _, st = gpu_fwd(desc, bufs, cfg["S"], cfg["order"], cfg["causal"], T, out_dtype=out_dtype, count=False)
+    assert st == 0
+    ref, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, cfg["S"], cfg["order"], cfg["causal"], T)
+    if cfg["bf16_out"]:
+        ref = oracle_bf16(ref)
+    o = o_to_numpy(O).reshape(B * Hq, N, d)
+    assert np.all(np.isfinite(o))
+    assert rel_f(o, ref).max() <= REL_F_TOL
