@@ -1,5 +1,7 @@
-"""A seeded sweep of random option combinations, each run end to end on the
-GPU and checked against the oracle: shapes (B, GQA group, ragged N, d), KV
+"""Seeded sweeps of random option combinations on the GPU, checked against the
+oracle: attnq_prepare alone (ragged lengths from 1, value scales from 1e-30 to
+1e30, outlier channels; bit-exact), attnq_fwd_ponly (any S; outputs and
+underflow counts), and the whole path end to end: shapes (B, GQA group, ragged N, d), KV
 tile, order, causal or not, P-cast scale, rotation and centring, input and
 output types, per-tile scales and causal-prefix statistics, INT8 Q/K codes.
 The structured tests cover each option on its own; this covers them mixed.
@@ -70,3 +72,85 @@ def test_random_option_mix(cfg):
     o = o_to_numpy(O).reshape(B * Hq, N, d)
     assert np.all(np.isfinite(o))
     assert rel_f(o, ref).max() <= REL_F_TOL
+
+
+def _prepare_configs(n, seed=7401):
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        Hkv = rng.choice([1, 2, 3])
+        c = dict(B=rng.choice([1, 2]), Hkv=Hkv, Hq=Hkv * rng.choice([1, 2, 4, 5]), N=rng.randint(1, 700),
+                 d=rng.choice([64, 128]), flags=rng.choice([0, ROT, CEN, ROT | CEN])
+                 | (TILE if rng.random() < 0.3 else 0) | (I8 if rng.random() < 0.3 else 0),
+                 f32_in=rng.random() < 0.4, vt=rng.random() < 0.7,
+                 scale=rng.choice([1.0, 1e-30, 1e-3, 1e3, 1e30]), outliers=rng.random() < 0.4, seed=8500 + i)
+        c["stat_len"] = rng.randint(1, c["N"]) if (rng.random() < 0.3 and not c["flags"] & TILE) else 0
+        out.append(c)
+    return out
+
+
+@pytest.mark.parametrize("cfg", _prepare_configs(40), ids=lambda c: f"p{c['seed']}")
+def test_random_prepare_mix(cfg):
+    """attnq_prepare over random option mixes, ragged lengths from 1 and value
+    scales from 1e-30 to 1e30 (fp32 inputs; bf16 inputs take the scale too,
+    as far as bf16 reaches), with and without large outlier channels: every
+    code, descale and mean-key value equal to the oracle's."""
+    from tests.gpu_helpers import gpu_prepare, prepared_to_numpy
+    B, Hq, Hkv, N, d = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"]
+    q, k, v = synth.qkv_normal(cfg["seed"], B, Hq, Hkv, N, d)
+    q, k, v = (x * np.float32(cfg["scale"]) for x in (q, k, v))
+    if cfg["outliers"]:
+        ch = synth.pick_channels(cfg["seed"], d, 2)
+        q[..., ch] *= np.float32(40.0)
+        k[..., ch] += np.float32(30.0 * cfg["scale"])
+    if not cfg["f32_in"]:
+        q, k, v = synth.to_bf16_bits(q), synth.to_bf16_bits(k), synth.to_bf16_bits(v)
+    flags = cfg["flags"]
+    signs = synth.hadamard_signs(cfg["seed"] + 1, d) if flags & ROT else None
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs, vt=cfg["vt"], stat_len=cfg["stat_len"])
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs, stat_len=cfg["stat_len"])
+    assert st == 0
+    got = prepared_to_numpy(desc, bufs)
+    for key in ("q8", "k8", "v8"):
+        assert np.array_equal(got[key], prep[key]), key
+    for key in ("q_descale", "k_descale", "v_descale"):
+        assert np.array_equal(got[key].view(np.uint32), prep[key].view(np.uint32)), key
+    if flags & CEN:
+        assert np.array_equal(got["k_mean"].view(np.uint32), prep["k_mean"].view(np.uint32))
+    if cfg["vt"]:
+        assert not got["v8_pad"].any()
+
+
+def _ponly_configs(n, seed=7501):
+    rng = random.Random(seed)
+    out = []
+    for i in range(n):
+        Hkv = rng.choice([1, 2])
+        out.append(dict(B=rng.choice([1, 2]), Hkv=Hkv, Hq=Hkv * rng.choice([1, 2, 3]), N=rng.randint(256, 1100),
+                        d=rng.choice([64, 128]), T=rng.choice([64, 128]), order=rng.choice([0, 1]),
+                        causal=rng.random() < 0.8, S=rng.choice([1.0, 256.0, 448.0, 100.0, 3.0]),
+                        delta=rng.choice([0.0, 4.0, 7.0, 12.0]), k_sink=rng.choice([0, 4, 9]), seed=8800 + i))
+    return out
+
+
+@pytest.mark.parametrize("cfg", _ponly_configs(24), ids=lambda c: f"q{c['seed']}")
+def test_random_ponly_mix(cfg):
+    """attnq_fwd_ponly (fp32 operands, only P cast, P and P * S in two steps,
+    so any S in (0, 448] is accepted) over random shapes, orders, scales, sink
+    strengths and sink counts: outputs within the forward tolerance and
+    underflow counts within 0.1 % + 2 of the oracle's."""
+    import precision_attention_numerics_gb300 as aq
+    from tests.gpu_helpers import REL_F_TOL, dev, rel_f
+    B, Hq, Hkv, N, d, T = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["N"], cfg["d"], cfg["T"]
+    q, k, v = synth.sink_inputs(cfg["seed"], B, Hq, N, d, delta=cfg["delta"])
+    k, v = k[:, ::Hq // Hkv].copy(), v[:, ::Hq // Hkv].copy()
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_F32, 0, None)
+    O = torch.empty((B, Hq, N, d), dtype=torch.float32, device="cuda")
+    uf = torch.zeros(B * Hq * 2, dtype=torch.int64, device="cuda")
+    aq.attnq_fwd_ponly(desc, dev(q), dev(k), dev(v), cfg["S"], cfg["order"], cfg["causal"], T, O, uf, cfg["k_sink"])
+    assert aq.attnq_device_status() == 0
+    got = O.cpu().numpy().astype(np.float64).reshape(B * Hq, N, d)
+    ref, uref = oracle.attn_ponly(q, k, v, cfg["S"], cfg["order"], cfg["causal"], T, k_sink=cfg["k_sink"])
+    assert rel_f(got, ref).max() <= REL_F_TOL
+    u = uf.cpu().numpy().reshape(-1, 2).astype(np.float64)
+    assert np.all(np.abs(u - uref.astype(np.float64)) <= 0.001 * uref.astype(np.float64) + 2)
