@@ -78,3 +78,39 @@ def test_host_pipeline_rejects_bad_arguments():
         aq.attnq_attention_host(desc, [x], [x[:, :1]], [x[:, :1]], 256.0, 1, True, 128, [o], aq.ATTNQ_BF16,
                                 ws[:256], torch.cuda.Stream(), s1, s2)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,d,T,f32_in,order", [(2, 6, 2, 333, 64, 64, True, 0), (1, 3, 3, 129, 128, 64, False, 1),
+                                                         (3, 5, 1, 700, 64, 128, True, 1)])
+def test_host_pipeline_shapes(B, Hq, Hkv, N, d, T, f32_in, order):
+    """Other shapes, fp32 inputs, 64-key tiles and the forward order through the
+    pipeline: its buffer sizes follow the shape and input type, and every step
+    equals the device path bit for bit."""
+    import precision_attention_numerics_gb300 as aq
+    steps = 3
+    flags = aq.ATTNQ_ROTATE | aq.ATTNQ_CENTER_K | aq.ATTNQ_VT_LAYOUT
+    signs = torch.from_numpy(synth.hadamard_signs(23, d)).cuda()
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_F32 if f32_in else aq.ATTNQ_BF16, flags, signs)
+    hosts = []
+    for i in range(steps):
+        q, k, v = synth.qkv_normal(7100 + i, B, Hq, Hkv, N, d)
+        if f32_in:
+            hosts.append(tuple(torch.from_numpy(x).pin_memory() for x in (q, k, v)))
+        else:
+            hosts.append(tuple(torch.from_numpy(synth.to_bf16_bits(x)).view(torch.bfloat16).pin_memory()
+                               for x in (q, k, v)))
+    outs = [torch.full((B, Hq, N, d), float("nan"), dtype=torch.float32).pin_memory() for _ in range(steps)]
+    ws = torch.empty(aq.attnq_host_pipeline_workspace(desc, aq.ATTNQ_F32), dtype=torch.uint8, device="cuda")
+    compute, cin, cout = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    aq.attnq_attention_host(desc, [h[0] for h in hosts], [h[1] for h in hosts], [h[2] for h in hosts], 448.0,
+                            order, True, T, outs, aq.ATTNQ_F32, ws, compute, cin, cout)
+    compute.synchronize()
+    assert aq.attnq_device_status(compute.cuda_stream) == 0
+    bufs = aq.alloc_prepared(desc)
+    for i in range(steps):
+        Q, K, V = (x.cuda() for x in hosts[i])
+        O = torch.empty((B, Hq, N, d), dtype=torch.float32, device="cuda")
+        aq.attnq_prepare(desc, Q, K, V, bufs.q8, bufs.k8, bufs.v8, bufs.scales, bufs.workspace)
+        aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, 448.0, order, True, T, O)
+        torch.cuda.synchronize()
+        assert np.array_equal(outs[i].view(torch.int32).numpy(), O.cpu().view(torch.int32).numpy()), i
