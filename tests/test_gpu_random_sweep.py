@@ -154,3 +154,31 @@ def test_random_ponly_mix(cfg):
     assert rel_f(got, ref).max() <= REL_F_TOL
     u = uf.cpu().numpy().reshape(-1, 2).astype(np.float64)
     assert np.all(np.abs(u - uref.astype(np.float64)) <= 0.001 * uref.astype(np.float64) + 2)
+
+
+@pytest.mark.parametrize("scale", [1e-20, 1e-3, 0.3, 3.0, 30.0])
+@pytest.mark.parametrize("order,flags", [(1, ROT | CEN), (0, 0), (1, I8 | ROT)])
+def test_forward_across_logit_scales(scale, order, flags):
+    """The whole path with inputs scaled so the logits go from below 2^-100
+    (every P is 1; the logit factor is raised to FLT_MIN) to several thousand
+    (one P per row), on 64-key tiles and a ragged N: outputs within the forward
+    tolerance of the oracle's emulation.  The kernel's exponent
+    fma(s, c, log2 S - m') uses the exact product s c where the oracle rounds
+    t = fl32(s c) first; each P then differs by a relative |t| 2^-25 at most,
+    under 1e-4 up to |t| = 2^12 (here |t| reaches 6.7e3 at scale 30), while at
+    scale 1e3 (|t| near 7.5e6) the outputs differ by 2.8e-2 - the amount a CPU
+    restatement of the fused form with an exact exp2 gives as well."""
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, rel_f
+    B, Hq, Hkv, N, d, T = 1, 4, 2, 517, 64, 64
+    q, k, v = synth.qkv_normal(9100, B, Hq, Hkv, N, d)
+    q, k = q * np.float32(scale), k * np.float32(scale)
+    signs = synth.hadamard_signs(9101, d) if flags & ROT else None
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    O, _, st = gpu_fwd(desc, bufs, 256.0, order, True, T, count=False)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs)
+    ref, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, order, True, T)
+    o = o_to_numpy(O).reshape(B * Hq, N, d)
+    assert np.all(np.isfinite(o))
+    assert rel_f(o, ref).max() <= REL_F_TOL
