@@ -221,7 +221,10 @@ attnq_status attnq_prepare_static(const attnq_desc* desc, const void* Q, const v
  * P_j * S, which equals S * l up to rounding; the cast and the division by
  * S * l are as stated.  E4M3 codes, and so the underflow counts, can
  * therefore differ from the literal two-step P then P * S where P * S lies
- * within a few ulp of a rounding boundary.  A factor c below the smallest
+ * within a few ulp of a rounding boundary.  The fma takes the exact product
+ * s_j * c where the two-step form rounds t_j to fp32 first: each P differs
+ * from it by a relative |t_j| * 2^-25 at most (t in log2 units), under 1e-4
+ * for |t_j| < 2^12.  A factor c below the smallest
  * normal float (FLT_MIN) is raised to FLT_MIN: every logit is then below
  * 2^-100 in magnitude either way (|s_j| < 2^25) and every P is 1 in fp32, so no result
  * changes, and masked keys keep P * S = 0.  A factor above the largest
