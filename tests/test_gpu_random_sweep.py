@@ -182,3 +182,44 @@ def test_forward_across_logit_scales(scale, order, flags):
     o = o_to_numpy(O).reshape(B * Hq, N, d)
     assert np.all(np.isfinite(o))
     assert rel_f(o, ref).max() <= REL_F_TOL
+
+
+@pytest.mark.parametrize("case", ["zero_q_tile", "zero_k_slice", "zero_v", "zero_q_tile_tiles", "constant_k"])
+def test_degenerate_inputs(case):
+    """Inputs with nothing to scale: a query tile of zeros (its amax is 0, so
+    its scale and descale are 1), a whole K slice of zeros (every logit 0:
+    uniform attention), V of zeros (O = 0), per-tile scales over a zero tile,
+    and K constant over the sequence (centring leaves zeros).  Codes and
+    descales equal the oracle's, outputs within the forward tolerance."""
+    from tests.gpu_helpers import REL_F_TOL, gpu_fwd, gpu_prepare, o_to_numpy, prepared_to_numpy, rel_f
+    B, Hq, Hkv, N, d, T = 1, 4, 2, 300, 64, 128
+    q, k, v = synth.qkv_normal(9200, B, Hq, Hkv, N, d)
+    flags = ROT | CEN
+    if case in ("zero_q_tile", "zero_q_tile_tiles"):
+        q[:, :, 128:256] = 0.0
+        if case == "zero_q_tile_tiles":
+            flags |= TILE
+    elif case == "zero_k_slice":
+        k[:, 1] = 0.0
+    elif case == "zero_v":
+        v[:] = 0.0
+    elif case == "constant_k":
+        k[:] = k[:, :, :1, :]
+    signs = synth.hadamard_signs(9201, d)
+    desc, bufs, st = gpu_prepare(q, k, v, flags, signs)
+    assert st == 0
+    prep = oracle.prepare(q, k, v, flags=flags, signs=signs)
+    got = prepared_to_numpy(desc, bufs)
+    for key in ("q8", "k8", "v8"):
+        assert np.array_equal(got[key], prep[key]), key
+    for key in ("q_descale", "k_descale", "v_descale"):
+        assert np.array_equal(got[key].view(np.uint32), prep[key].view(np.uint32)), key
+    O, _, st = gpu_fwd(desc, bufs, 256.0, 1, True, T, count=False)
+    assert st == 0
+    ref, _ = oracle.attn_quant(prep, (B, Hq, Hkv, N, d), flags, 256.0, 1, True, T)
+    o = o_to_numpy(O).reshape(B * Hq, N, d)
+    assert np.all(np.isfinite(o))
+    if case == "zero_v":
+        assert not o.any() and not ref.any()
+    else:
+        assert rel_f(o, ref).max() <= REL_F_TOL
