@@ -223,3 +223,24 @@ def test_degenerate_inputs(case):
         assert not o.any() and not ref.any()
     else:
         assert rel_f(o, ref).max() <= REL_F_TOL
+
+
+@pytest.mark.parametrize("B,Hq,N,d,bf16", [(1, 1, 1, 64, False), (3, 5, 2, 128, True), (1, 37, 1000, 64, False),
+                                           (2, 3, 4097, 128, True), (1, 2, 33333, 64, False)])
+def test_err_sizes(B, Hq, N, d, bf16):
+    """attnq_err (fp64 sums over an 8-CTA cluster per head) from one row of 64
+    values per head to two million values per head, fp32 and bf16 outputs:
+    equal to the oracle's error to 1e-10 relative."""
+    import precision_attention_numerics_gb300 as aq
+    n = B * Hq * N * d
+    ref = synth.normals(9300 + N, n).reshape(B, Hq, N, d).astype(np.float64)
+    noise = synth.normals(9301 + N, n).reshape(B, Hq, N, d).astype(np.float64)
+    scale = np.geomspace(1e-6, 0.5, B * Hq).reshape(B, Hq, 1, 1)
+    O = torch.from_numpy((ref + noise * scale).astype(np.float32)).cuda()
+    if bf16:
+        O = O.to(torch.bfloat16)
+    err = torch.empty(B * Hq, dtype=torch.float64, device="cuda")
+    aq.attnq_err(aq.AttnqDesc(B, Hq, Hq, N, d, aq.ATTNQ_F32, 0, None), O, torch.from_numpy(ref).cuda(), err)
+    assert aq.attnq_device_status() == 0
+    want = oracle.err(O.float().cpu().numpy().astype(np.float64).reshape(B * Hq, -1), ref.reshape(B * Hq, -1))
+    np.testing.assert_allclose(err.cpu().numpy(), want, rtol=1e-10, atol=1e-15)
