@@ -244,3 +244,43 @@ def test_err_sizes(B, Hq, N, d, bf16):
     assert aq.attnq_device_status() == 0
     want = oracle.err(O.float().cpu().numpy().astype(np.float64).reshape(B * Hq, -1), ref.reshape(B * Hq, -1))
     np.testing.assert_allclose(err.cpu().numpy(), want, rtol=1e-10, atol=1e-15)
+
+
+def test_concurrent_calls_on_two_streams():
+    """Two problems prepared and attended at the same time on two streams, each
+    with its own buffers and workspace (the library keeps no other state than
+    the status word): both results equal, bit for bit, the same calls made
+    one after the other."""
+    import precision_attention_numerics_gb300 as aq
+    shapes = [(1, 8, 2, 3000, 128), (2, 6, 3, 1777, 64)]
+    descs, inputs, outs_seq, outs_par, bufs = [], [], [], [], []
+    for n, (B, Hq, Hkv, N, d) in enumerate(shapes):
+        q, k, v = synth.qkv_normal(9400 + n, B, Hq, Hkv, N, d)
+        signs = torch.from_numpy(synth.hadamard_signs(9410 + n, d)).cuda()
+        desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_F32, ROT | CEN | aq.ATTNQ_VT_LAYOUT, signs)
+        descs.append(desc)
+        inputs.append(tuple(torch.from_numpy(x).cuda() for x in (q, k, v)))
+        bufs.append(aq.alloc_prepared(desc))
+    for n, desc in enumerate(descs):
+        B, Hq, Hkv, N, d = shapes[n]
+        O = torch.empty((B, Hq, N, d), device="cuda")
+        aq.attnq_prepare(desc, *inputs[n], bufs[n].q8, bufs[n].k8, bufs[n].v8, bufs[n].scales, bufs[n].workspace)
+        aq.attnq_fwd(desc, bufs[n].q8, bufs[n].k8, bufs[n].v8, bufs[n].scales, 256.0, 1, True, 128, O)
+        torch.cuda.synchronize()
+        outs_seq.append(O.cpu())
+    bufs2 = [aq.alloc_prepared(desc) for desc in descs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for n, desc in enumerate(descs):
+        B, Hq, Hkv, N, d = shapes[n]
+        with torch.cuda.stream(streams[n]):
+            O = torch.empty((B, Hq, N, d), device="cuda")
+            # the binding launches on the current stream: streams[n]
+            aq.attnq_prepare(desc, *inputs[n], bufs2[n].q8, bufs2[n].k8, bufs2[n].v8, bufs2[n].scales,
+                             bufs2[n].workspace)
+            aq.attnq_fwd(desc, bufs2[n].q8, bufs2[n].k8, bufs2[n].v8, bufs2[n].scales, 256.0, 1, True, 128, O)
+            outs_par.append(O)
+    torch.cuda.synchronize()
+    assert aq.attnq_device_status() == 0
+    for n in range(2):
+        assert torch.equal(outs_par[n].cpu().view(torch.int32), outs_seq[n].view(torch.int32)), n
