@@ -284,3 +284,46 @@ def test_concurrent_calls_on_two_streams():
     assert aq.attnq_device_status() == 0
     for n in range(2):
         assert torch.equal(outs_par[n].cpu().view(torch.int32), outs_seq[n].view(torch.int32)), n
+
+
+def test_cuda_graph_capture_and_replay():
+    """prepare + attention captured once in a CUDA graph and replayed on new
+    inputs written into the captured buffers: every replay equals the direct
+    calls on the same inputs bit for bit (the launches take no host state that
+    changes between calls)."""
+    import precision_attention_numerics_gb300 as aq
+    B, Hq, Hkv, N, d, T = 1, 6, 2, 1000, 128, 128
+    signs = torch.from_numpy(synth.hadamard_signs(9501, d)).cuda()
+    desc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, ROT | CEN | aq.ATTNQ_VT_LAYOUT, signs)
+
+    def inputs(seed):
+        return tuple(torch.from_numpy(synth.to_bf16_bits(x)).view(torch.bfloat16).cuda()
+                     for x in synth.qkv_normal(seed, B, Hq, Hkv, N, d))
+
+    Q, K, V = inputs(9500)
+    bufs = aq.alloc_prepared(desc)
+    O = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device="cuda")
+
+    def step():
+        aq.attnq_prepare(desc, Q, K, V, bufs.q8, bufs.k8, bufs.v8, bufs.scales, bufs.workspace)
+        aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, 256.0, 1, True, T, O)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for seed in (9510, 9511, 9512):
+        Qn, Kn, Vn = inputs(seed)
+        Q.copy_(Qn); K.copy_(Kn); V.copy_(Vn)
+        g.replay()
+        torch.cuda.synchronize()
+        got = O.clone()
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), O.view(torch.int16)), seed
+    assert aq.attnq_device_status() == 0
