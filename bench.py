@@ -440,6 +440,25 @@ def _event_ms(fn, warmup, steps, stream):
     return e0.elapsed_time(e1) / steps
 
 
+def _graph_ms(fn, warmup, steps, stream):
+    """Mean device time of one replay of a CUDA graph holding fn()'s launches
+    (captured once after `warmup` direct calls): the same kernels without the
+    per-call host work, for workloads whose kernels last a few microseconds."""
+    import torch
+    for _ in range(max(1, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    return _event_ms(g.replay, 2, steps, stream)
+
+
 def nonsink_in_mask(N: int, k_sink: int) -> int:
     """In-mask keys j >= k_sink summed over the N query rows of one causal head."""
     r = np.arange(N, dtype=np.int64)
@@ -486,7 +505,8 @@ def run_config1(args):
         for S in wl["S"]:
             aq.attnq_fwd(desc, bufs.q8, bufs.k8, bufs.v8, bufs.scales, S, aq.ATTNQ_KV_FORWARD, True, T, Os[S])
 
-    ms = _event_ms(step, args.warmup, args.steps, stream)
+    ms_direct = _event_ms(step, args.warmup, args.steps, stream)
+    ms = _graph_ms(step, args.warmup, args.steps, stream)
     flops = attn_flops(B, H, N, d) * len(wl["S"])
     # one untimed pass with the underflow counters, and the per-head error
     # against the GPU's FP64 reference
@@ -528,9 +548,11 @@ def run_config1(args):
                "cores": oracle.threads(), "kind": "oracle", "sample": "the whole workload", "parity": parity}
     cfg = {"workload": "sink_probe", "B": B, "H": H, "N": N, "d": d, "kv_tile": T, "in_dtype": "f32",
            "delta": wl["deltas"][0], "S": list(wl["S"]), "kv_order": "forward", "rotate": False, "center_k": False,
-           "step": "attnq_prepare + attnq_fwd (S=1) + attnq_fwd (S=256)", "l2": "inputs fit in L2 (launch-bound size)"}
+           "step": "attnq_prepare + attnq_fwd (S=1) + attnq_fwd (S=256)", "l2": "inputs fit in L2 (launch-bound size)",
+           "launch": "one CUDA graph replay per step (ms_per_step_direct: the same calls made directly)"}
     line = _common_line("sink probe step time (launch-bound)", ms * 1e3, "us per step", args, False, "e4m3", cfg,
-                        ms_per_step=ms, tflops=flops / (ms * 1e-3) / 1e12, per_S=per_s, cpu_baseline=cpu,
+                        ms_per_step=ms, ms_per_step_direct=ms_direct, tflops=flops / (ms * 1e-3) / 1e12,
+                        per_S=per_s, cpu_baseline=cpu,
                         gpu_launches=args.steps * (2 + len(wl["S"])))
     print(json.dumps(line), flush=True)
     return 0
@@ -727,7 +749,8 @@ def run_config34(args, name):
                 aq.attnq_prepare(ds, Q, K, V, bf.q8, bf.k8, bf.v8, bf.scales, bf.workspace)
                 aq.attnq_fwd(ds, bf.q8, bf.k8, bf.v8, bf.scales, 256.0, aq.ATTNQ_KV_REVERSE, True, T, O)
 
-    ms_fp8 = _event_ms(fp8_step, args.warmup, args.steps, stream)
+    ms_fp8_direct = _event_ms(fp8_step, args.warmup, args.steps, stream)
+    ms_fp8 = _graph_ms(fp8_step, args.warmup, args.steps, stream)
     flops = attn_flops(B, Hq, N, d) * L * len(conds)
     rdesc = aq.AttnqDesc(B, Hq, Hkv, N, d, aq.ATTNQ_BF16, 0, signs)
     ws = torch.empty(aq.attnq_harm_workspace(rdesc), dtype=torch.uint8, device=dev)
@@ -764,10 +787,12 @@ def run_config34(args, name):
                "parity": {"max_rel_err_diff_per_head": worst, "bar": 0.05}}
     cfg = {"workload": name, "layers": L, "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "kv_tile": T, "S": 256.0,
            "kv_order": "reverse", "in_dtype": "bf16", "out_dtype": "f32", "conditions": [c for c, _ in conds],
-           "step": "attnq_prepare + attnq_fwd for every layer and condition", "l2": "no flush (layers rotate through L2)"}
+           "step": "attnq_prepare + attnq_fwd for every layer and condition", "l2": "no flush (layers rotate through L2)",
+           "launch": "one CUDA graph replay per step (ms_per_step_direct: the same calls made directly)"}
     line = _common_line("causal FP8 attention fwd TFLOP/s over all layers and conditions; per-head log1p rel-F vs FP64",
                         flops / (ms_fp8 * 1e-3) / 1e12, "TFLOP/s", args, True, "e4m3", cfg,
-                        ms_per_step=ms_fp8, harm_report_ms_per_layer=ms_harm / L,
+                        ms_per_step=ms_fp8, ms_per_step_direct=ms_fp8_direct,
+                        tflops_direct=flops / (ms_fp8_direct * 1e-3) / 1e12, harm_report_ms_per_layer=ms_harm / L,
                         mean_log1p_relF=summary, heads=int(L * Hq),
                         heads_harmed_by_rotation=int(np.sum(harm > 0)), cpu_baseline=cpu,
                         gpu_launches=args.steps * L * len(conds) * 3)
