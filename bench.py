@@ -34,8 +34,10 @@ four-condition harm report on one Qwen-0.5B-shaped layer instead.
 The other workloads, one JSON line each: --config 1 (sink probe), 2 (P-cast
 isolation sweep: MSE and underflow fraction of all 78 runs, --report-md
 writes the table), 3 and 4 (every layer of the Qwen-0.5B- and 1.5B-shaped
-workloads in all four conditions); each times the GPU and, in its
-cpu_baseline leg, the oracle on the whole workload, with parity figures.
+workloads in all four conditions); each times the GPU (configs 1, 3 and 4,
+whose kernels last microseconds, as one CUDA graph replay per step, with the
+direct-call time beside it) and, in its cpu_baseline leg, the oracle on the
+whole workload, with parity figures.
 
 --impl reference times the CPU oracle (the plain C++ implementation used by
 the tests) on a bounded sample of the same workload.
