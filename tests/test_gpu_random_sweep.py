@@ -15,7 +15,10 @@ rounding point can take the other code under the hardware exp2 (its rare,
 documented difference from the oracle's exact exp2), and in a head of a few
 dozen keys per row one such code moves the head's relative error by about
 2e-3 by itself (N = 67 gave 2.4e-3; perturbing the oracle's exp2 by 2^-22
-reproduces it to the last digit); over hundreds of keys per row it does not."""
+reproduces it to the last digit); with hundreds of rows the short rows are a
+small share of the head.  (An exploratory run of 300 such configurations found
+one more: S = 96, N = 318, where the oracle's second rounding, of P * S, lands
+exactly on an E4M3 midpoint; see the exp reading in the design notes.)"""
 import random
 
 import numpy as np
